@@ -1,0 +1,431 @@
+"""Benchmark of the QuantMLA decode path (libmlaq) on synthetic inputs.
+
+One step = the whole hot path for one batch: the fused writer appends one new
+token to every sequence (mlaq_append), then split-KV decode attention runs
+over the mixed-precision paged cache (mlaq_decode: planner, attention kernel,
+combine). Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl mlaq|reference]
+
+value = effective cache GB/s = algorithmic bytes per step / device time per
+step (inputs resident in HBM, L2 flushed between timed steps). The algorithmic
+bytes of a decode step are sum_b [min(L_b,132) * 1152 + max(0, L_b-132) * P]
++ B*H*(1152 + 1024 + 4), P = packed bytes + fp16 meta per token (C4R4 324,
+C2R4 196, BF16 1152); the append adds B * (1152 read + P + 1152) bytes.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "decode-attn µs/step & effective cache GB/s (C4R4/C2R4), % of roofline"
+PACKED_TOKEN_BYTES = {"C4R4": 288 + 36, "C2R4": 160 + 36, "BF16": 1152}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def decode_bytes(seq_lens, mode, B, H):
+    P = PACKED_TOKEN_BYTES[mode]
+    tot = 0
+    for L in seq_lens:
+        if mode == "BF16":
+            tot += L * 1152
+        else:
+            tot += min(L, 132) * 1152 + max(0, L - 132) * P
+    return tot + B * H * (1152 + 1024 + 4)
+
+
+def append_bytes(B, mode):
+    P = PACKED_TOKEN_BYTES[mode]
+    return B * (1152 + P + (0 if mode == "BF16" else 1152))
+
+
+def decode_flops(seq_lens, H):
+    return sum(seq_lens) * 2 * H * (576 + 512)
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return pk["hbm_gbs"], pk["bf16_tflops"], pk.get("bf16_tflops_sustained", pk["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in ("mlaq_decode.cu", "mlaq_internal.cuh"):
+        with open(os.path.join(ROOT, "bit_mla_kv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the decode kernel from a committed ncu summary,
+    or None when absent or taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", "decode_kernel_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    ent = rec.get(workload)
+    if not ent or ent.get("kernel_source_sha") != kernel_source_sha():
+        return None
+    return ent.get("traffic_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 7:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[3 + k].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "mlaq" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def oracle_sample(case_tokens, seq_lens, queries, mode, budget_s):
+    """Time the oracle (as it stands) on whole sequences until ~budget_s of CPU
+    work. case_tokens(b) -> [L, 576] float32. Returns (bytes, seconds, desc)."""
+    import oracle as O
+    done_bytes, t_total, seqs, toks = 0, 0.0, [], 0
+    order = sorted(range(len(seq_lens)), key=lambda b: seq_lens[b])
+    order = order[len(order) // 2:] + order[:len(order) // 2]  # start near the median length
+    ql, qr = queries
+    for b in order:
+        L = seq_lens[b]
+        tok = case_tokens(b)
+        codes = meta = None
+        if mode != "BF16":
+            codes, meta = O.quantize_tokens(tok[:, :512], tok[:, 512:], mode)  # cache state, not timed
+        t0 = time.perf_counter()
+        O.decode_sequence(ql[b], qr[b], tok, codes, meta, L, W.SOFTMAX_SCALE, mode)
+        t_total += time.perf_counter() - t0
+        done_bytes += decode_bytes([L], mode, 1, ql.shape[1])
+        seqs.append(b)
+        toks += L
+        if t_total >= budget_s:
+            break
+    return done_bytes, t_total, f"{len(seqs)} whole sequences ({toks} tokens, H={ql.shape[1]})"
+
+
+def cores_used():
+    try:
+        n = len(os.sched_getaffinity(0))
+    except Exception:
+        n = os.cpu_count() or 1
+    return n
+
+
+def build_inputs(wl, rank, device, total_steps):
+    """Seeded inputs on the device for one replica."""
+    seed = wl.seed + 1000 * rank
+    stats = W.CacheStats(seed)
+    g = W.generator(seed, device)
+    c, k, cu = W.make_sequences(wl.seq_lens, stats, g, device)
+    ql, qr = W.make_queries(wl.B, wl.H, g, device)
+    cn, kn = W.make_tokens(wl.B * total_steps, stats, g, device)
+    cn = cn.view(total_steps, wl.B, 1, 512)
+    kn = kn.view(total_steps, wl.B, 1, 64)
+    pt, num_pages = W.make_page_table([L + total_steps + 64 for L in wl.seq_lens], seed)
+    return dict(c=c, k=k, cu=cu, ql=ql, qr=qr, cn=cn, kn=kn, pt=pt.to(device), num_pages=num_pages, seed=seed)
+
+
+def run_mlaq(args, ws, rank, local):
+    from bit_mla_kv_gb300 import build as B
+    B.build()
+    from bit_mla_kv_gb300.mlaq import Cache
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    wl = W.workload(args.workload)
+    K, Wm = args.steps, args.warmup
+    inp = build_inputs(wl, rank, device, K + Wm + K)  # warmup + timed + e2e steps
+    cache = Cache(wl.mode, inp["num_pages"], wl.B, inp["pt"].shape[1], max_heads=max(wl.H, 16), device=device)
+    seq = torch.zeros(wl.B, dtype=torch.int32, device=device)
+    cache.append(inp["pt"], seq, inp["c"], inp["k"], cu_new=inp["cu"].to(device))
+    torch.cuda.synchronize()
+    assert cache.device_status() == 0, "writer reported a device error"
+    out = torch.empty(wl.B, wl.H, 512, dtype=torch.bfloat16, device=device)
+    lse = torch.empty(wl.B, wl.H, dtype=torch.float32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def step(i):
+        cache.append(inp["pt"], seq, inp["cn"][i], inp["kn"][i])
+        cache.decode(inp["ql"], inp["qr"], inp["pt"], seq, W.SOFTMAX_SCALE, out=out, lse=lse)
+
+    for i in range(Wm):
+        flush.zero_()
+        step(i)
+    torch.cuda.synchronize()
+    lens_at_start = [int(x) for x in seq.cpu().tolist()]
+    cache.timing_enable(K)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(ws)
+    torch.cuda.synchronize()
+    for j in range(K):
+        flush.zero_()
+        evs[j][0].record()
+        step(Wm + j)
+        evs[j][1].record()
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    kern_ms = cache.timing_read()
+    ms = sum(step_ms) / K
+    ms_max = max_over_ranks(ms, ws, device)
+    mean_lens = [L + (K - 1) / 2.0 for L in lens_at_start]
+    bytes_step = decode_bytes(mean_lens, wl.mode, wl.B, wl.H) + append_bytes(wl.B, wl.mode)
+    dec_bytes = decode_bytes(mean_lens, wl.mode, wl.B, wl.H)
+    bytes_all = sum_over_ranks(bytes_step, ws, device)
+    value = bytes_all / (ms_max * 1e-3) / 1e9
+    kern_avg = sum(kern_ms) / max(len(kern_ms), 1)
+    hbm, tf_burst, tf_sus, peak_src = load_peaks()
+    flops = decode_flops(mean_lens, wl.H)
+    t_mem = dec_bytes / (hbm * 1e9)
+    t_ten = flops / (tf_burst * 1e12)
+    bound = "hbm" if t_mem >= t_ten else "tensor"
+    if bound == "hbm":
+        achieved = dec_bytes / (kern_avg * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "peak_source": f"{peak_src} hbm_gbs (copy)"}
+    else:
+        achieved = flops / (kern_avg * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tf_burst, "unit": "TFLOP/s",
+                "frac": achieved / tf_burst, "peak_source": f"{peak_src} bf16_tflops (burst)"}
+    roof["traffic"] = recorded_traffic(args.workload)
+    roof["kernel"] = "mlaq::decode_kernel (split-KV attention)"
+    roof["kernel_ms"] = kern_avg
+    roof["roofline_us"] = max(t_mem, t_ten) * 1e6
+    roof["frac_of_roofline_kernel"] = max(t_mem, t_ten) * 1e3 / kern_avg
+
+    # ---- end to end through the public API with host buffers
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    h_ql, h_qr = pin(inp["ql"]), pin(inp["qr"])
+    h_cn = pin(inp["cn"][Wm + K:])
+    h_kn = pin(inp["kn"][Wm + K:])
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    d_ql, d_qr = torch.empty_like(inp["ql"]), torch.empty_like(inp["qr"])
+    d_cn, d_kn = torch.empty_like(inp["cn"][0]), torch.empty_like(inp["kn"][0])
+    h2d = (h_ql.numel() * 2 + h_qr.numel() * 2 + d_cn.numel() * 2 + d_kn.numel() * 2)
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for j in range(K):
+        d_ql.copy_(h_ql, non_blocking=True)
+        d_qr.copy_(h_qr, non_blocking=True)
+        d_cn.copy_(h_cn[j], non_blocking=True)
+        d_kn.copy_(h_kn[j], non_blocking=True)
+        cache.append(inp["pt"], seq, d_cn, d_kn)
+        cache.decode(d_ql, d_qr, inp["pt"], seq, W.SOFTMAX_SCALE, out=out, lse=lse)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / K
+    barrier(ws)
+    e2e_s = max_over_ranks(e2e_s, ws, device)
+    e2e_val = bytes_all / e2e_s / 1e9
+    assert cache.device_status() == 0, "device error during the benchmark"
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        c_host, k_host, cu = inp["c"], inp["k"], inp["cu"]
+
+        def tokens(b):
+            a, e = int(cu[b]), int(cu[b + 1])
+            return torch.cat([c_host[a:e], k_host[a:e]], -1).float().cpu().numpy()
+
+        qs = (inp["ql"].float().cpu().numpy(), inp["qr"].float().cpu().numpy())
+        nb, secs, desc = oracle_sample(tokens, wl.seq_lens, qs, wl.mode, args.cpu_budget)
+        cpu = {"value": nb / secs / 1e9, "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
+               "sample": desc + f", {secs:.1f} s of fp64 NumPy decode (BLAS threads: default)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K, "warmup": Wm,
+        "ms_per_step": ms_max, "us_per_step": ms_max * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16 MMA operands (int4/int2 codes exact), f32 accumulate",
+        "data": "synthetic (seeded; N(0,1) latent with 8 outlier channels x10, RoPE pairs x10^U(-1,1))",
+        "config": {"workload": f"{wl.name}: {wl.description}", "mode": wl.mode, "B": wl.B, "H": wl.H,
+                   "tokens_at_start": sum(lens_at_start), "step": "mlaq_append (1 token/seq) + mlaq_decode",
+                   "l2": "flushed between timed steps (256 MiB write, outside the step events)",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": 5 * K,
+        "clocks": clocks,
+        "impl": "mlaq",
+    }
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def run_reference(args, ws, rank):
+    """The oracle, as it stands, on the host cores: each step decodes a bounded
+    sample of the workload's sequences."""
+    if rank != 0:
+        return
+    wl = W.workload(args.workload)
+    g = W.generator(wl.seed, "cpu")
+    stats = W.CacheStats(wl.seed)
+    # generate only the sampled sequences (the oracle never sees the rest)
+    order = sorted(range(wl.B), key=lambda b: wl.seq_lens[b])
+    ql, qr = W.make_queries(wl.B, wl.H, g)
+    qs = (ql.float().numpy(), qr.float().numpy())
+    cache = {}
+
+    def tokens(b):
+        if b not in cache:
+            gb = W.generator(wl.seed * 7 + b, "cpu")
+            c, k = W.make_tokens(wl.seq_lens[b], stats, gb)
+            cache[b] = torch.cat([c, k], -1).float().numpy()
+        return cache[b]
+
+    per = []
+    for i in range(args.warmup + args.steps):
+        nb, secs, desc = oracle_sample(tokens, wl.seq_lens, qs, wl.mode, args.ref_budget)
+        if i >= args.warmup:
+            per.append((nb, secs))
+    nb = sum(x for x, _ in per)
+    secs = sum(s for _, s in per)
+    val = nb / secs / 1e9
+    ms = secs / len(per) * 1e3
+    line = {
+        "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, same distributions)",
+        "config": {"workload": f"{wl.name}: {wl.description}", "mode": wl.mode, "B": wl.B, "H": wl.H,
+                   "step": "oracle decode of a bounded sample of the batch's sequences"},
+        "impl": "reference",
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
+                         "sample": desc + " per step"},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="v2lite_c4r4")
+    ap.add_argument("--impl", default="mlaq", choices=["mlaq", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=2.0, help="seconds of oracle work per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    ws, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_mlaq(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,203 @@
+// Internal definitions shared by the libmlaq kernels and the C-ABI layer.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mlaq.h"
+
+namespace mlaq {
+
+constexpr int kPage = 64;        // tokens per page
+constexpr int kSink = 4;         // sink tokens kept in BF16
+constexpr int kRecent = 128;     // recent tokens kept in BF16
+constexpr int kRing = kSink + kRecent;
+constexpr int kDL = 512;         // content latent width
+constexpr int kDR = 64;          // RoPE key width
+constexpr int kD = kDL + kDR;    // 576
+constexpr int kGroup = 64;       // quantization group
+constexpr int kGroups = kD / kGroup;  // 9 (8 content + 1 RoPE)
+constexpr int kMetaTok = kGroups * 4;  // bytes of (scale, min) fp16 pairs per token
+constexpr int kMetaPage = kPage * kMetaTok;  // 2304
+
+// Workspace layout (bytes from the workspace base).
+constexpr size_t kWsStatus = 0;          // int32 sticky status
+constexpr size_t kWsNumItems = 4;        // int32 number of work items of the last plan
+constexpr size_t kWsItems = 256;         // int4 items[max_items]
+constexpr int kMaxPlanCtas = 1024;       // decode CTA target never exceeds this
+
+__host__ __device__ constexpr int content_bits(int mode) { return mode == MLAQ_C2R4 ? 2 : 4; }
+// Bytes of codes per token in a page (BF16 mode: the raw token).
+__host__ __device__ constexpr int token_bytes(int mode) {
+  return mode == MLAQ_BF16 ? kD * 2 : (kDL * content_bits(mode) + kDR * 4) / 8;
+}
+__host__ __device__ constexpr int group_code_bytes(int bits) { return kGroup * bits / 8; }
+__host__ __device__ constexpr int page_code_bytes(int mode) { return kPage * token_bytes(mode); }
+
+inline size_t max_items_for(int max_seqs) { return (size_t)2 * max_seqs + kMaxPlanCtas; }
+// Rows (item, head) of the partial outputs: items * H <= 2 B H + 16 * ctas.
+inline size_t max_partial_rows(int max_seqs, int max_heads) {
+  return (size_t)2 * max_seqs * max_heads + (size_t)16 * kMaxPlanCtas;
+}
+
+// Work item of the split-KV decode: sequence b, kind (0 = packed / paged range
+// [tlo, thi), 1 = the sequence's BF16 sink + recent ring).
+struct Item {
+  int b, kind, tlo, thi;
+};
+
+// ---------------------------------------------------------------------------
+// Physical code layout inside a token's bytes.
+//
+// Per token: content groups g = 0..7 (32 B each for INT4, 16 B for INT2), then
+// the RoPE group (32 B, INT4). The channel order inside a group is permuted so
+// that one 64-bit (INT4) or 32-bit (INT2) shared-memory load gives a thread
+// exactly the fp16 pairs of the m16n8k16 B fragments it needs, and so that
+// a LOP3 with a 0x6400 exponent turns two codes into an fp16 pair (1024 + m*q)
+// without shifts. The canonical order (code i of the segment in bits
+// [b*(i mod k), +b) of byte i/k) is produced by mlaq_export_tokens.
+//
+// Shared notation: for channel c of a 64-channel group,
+//   kk = c >> 4 (MMA k-step), bi = (c >> 3) & 1 (B register b0/b1),
+//   i = (c >> 1) & 3 (thread in the quad), ln = c & 1 (fp16 lane in the pair).
+// Returns the bit offset of the code inside the group's bytes.
+__host__ __device__ inline int content_code_bit(int c, int bits) {
+  int kk = c >> 4, bi = (c >> 3) & 1, i = (c >> 1) & 3, ln = c & 1;
+  if (bits == 4) {
+    int word = 2 * i + (kk >> 1);
+    int p = 2 * (kk & 1) + bi;  // 0: bits 0-3, 1: 4-7, 2: 8-11, 3: 12-15 of each 16-bit lane
+    return word * 32 + 16 * ln + 4 * (p & 1) + 8 * (p >> 1);
+  } else {
+    int word = i;
+    int p = 2 * kk + bi;  // 0..7: 2-bit field (p & 3) of byte (p >> 2) of each 16-bit lane
+    return word * 32 + 16 * ln + 2 * (p & 3) + 8 * (p >> 2);
+  }
+}
+// RoPE group (INT4): warp w of the decode kernel owns k-step kk = w.
+__host__ __device__ inline int rope_code_bit(int c) {
+  int kk = c >> 4, bi = (c >> 3) & 1, i = (c >> 1) & 3, ln = c & 1;
+  int word = 2 * kk + (i >> 1);
+  return word * 32 + 16 * ln + 8 * (i & 1) + 4 * bi;
+}
+
+// ---------------------------------------------------------------------------
+// PTX helpers.
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: returns false if the phase did not complete within `limit` polls.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit) {
+  for (uint32_t n = 0; n < limit; ++n)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// Bulk (TMA) copy global -> shared, completion signalled on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Barrier that also ORs a predicate across the participating threads.
+__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(out)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return out != 0;
+}
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));  // (a & b) | c
+  return d;
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+// D += A * B, m16n8k16, fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+}  // namespace mlaq
+
+// Host-side handle.
+struct mlaq_cache {
+  int mode;
+  int32_t num_pages, max_seqs, max_pages_per_seq, max_heads;
+  void* codes;
+  void* meta;
+  void* ring;
+  void* workspace;
+  size_t workspace_bytes;
+  int num_sms;
+  int decode_ctas;
+  // timing
+  int timing_max;
+  int timing_n;
+  void** timing_events;  // cudaEvent_t pairs
+};
+
+// Kernel launchers (defined in the .cu files).
+namespace mlaq {
+cudaError_t launch_append(const mlaq_cache* c, const int32_t* page_table, int32_t* seq_lens, int B,
+                          const uint16_t* c_latent, const uint16_t* k_rope, int n_new, const int32_t* cu_new,
+                          int total_new, cudaStream_t s);
+cudaError_t launch_export(const mlaq_cache* c, const int32_t* page_table, int B, const int32_t* token_b,
+                          const int32_t* token_t, int n, uint8_t* codes_out, uint16_t* meta_out, cudaStream_t s);
+cudaError_t launch_decode(mlaq_cache* c, const uint16_t* q_latent, const uint16_t* q_rope,
+                          const int32_t* page_table, const int32_t* seq_lens, int B, int H, float scale,
+                          uint16_t* out, float* lse, cudaStream_t s);
+}  // namespace mlaq

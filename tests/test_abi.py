@@ -1,0 +1,94 @@
+"""CPU checks of the C-ABI library: it builds, loads, exports every symbol the
+header declares, and its host-side argument checks answer without a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mlaq.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_mla_kv_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mlaq_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("mlaq_append", "mlaq_decode", "mlaq_buffer_sizes", "mlaq_cache_create", "mlaq_export_tokens"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_the_exports():
+    import bit_mla_kv_gb300.mlaq as m
+    assert sorted(m.EXPORTED) == declared_functions()
+
+
+def test_buffer_sizes_host_logic(lib):
+    import bit_mla_kv_gb300.mlaq as m
+    cb, mb, rb, wb = m.buffer_sizes("C4R4", 10, 3, 16)
+    assert cb == 10 * 64 * 288 and mb == 10 * 64 * 36 and rb == 3 * 132 * 576 * 2
+    cb, mb, rb, wb2 = m.buffer_sizes("C2R4", 10, 3, 16)
+    assert cb == 10 * 64 * 160 and mb == 10 * 64 * 36 and wb2 == wb
+    cb, mb, rb, _ = m.buffer_sizes("BF16", 10, 3, 16)
+    assert cb == 10 * 64 * 1152 and mb == 0 and rb == 0
+    with pytest.raises(m.MlaqError):
+        m.buffer_sizes("C4R4", 10, 3, 24)   # heads not a multiple of 16
+    with pytest.raises(m.MlaqError):
+        m.buffer_sizes("C4R4", 0, 3, 16)
+
+
+def test_host_argument_errors(lib):
+    lib.mlaq_status_string.restype = ctypes.c_char_p
+    assert lib.mlaq_status_string(0) == b"ok"
+    out = ctypes.c_void_p()
+    # bad mode / sizes / NULL buffers are rejected before any CUDA call
+    assert lib.mlaq_cache_create(ctypes.byref(out), 7, 1, 1, 1, 16, None, None, None, None, ctypes.c_size_t(0)) == -2
+    assert lib.mlaq_cache_create(ctypes.byref(out), 0, 0, 1, 1, 16, None, None, None, None, ctypes.c_size_t(0)) == -3
+    assert lib.mlaq_cache_create(ctypes.byref(out), 0, 1, 1, 1, 16, None, None, None, None, ctypes.c_size_t(0)) == -1
+    buf = ctypes.create_string_buffer(64)
+    addr = (ctypes.addressof(buf) + 15) // 16 * 16
+    mis = ctypes.c_void_p(addr + 4)
+    assert lib.mlaq_cache_create(ctypes.byref(out), 0, 1, 1, 1, 16, mis, mis, mis, mis, ctypes.c_size_t(0)) == -4
+    assert lib.mlaq_decode(None, None, None, None, None, 1, 16, ctypes.c_float(1.0), None, None, None) == -1
+    assert lib.mlaq_append(None, None, None, 1, None, None, 1, None, 0, None) == -1
+
+
+def test_code_layout_is_a_bijection():
+    # The physical nibble/crumb positions of the 64 channels of a group must
+    # be distinct and fill the group's bytes (checked through the export
+    # path's inverse on the GPU; here the formula itself, mirrored in Python
+    # from the header comment, is checked for collisions).
+    def content_bit(c, bits):
+        kk, bi, i, ln = c >> 4, (c >> 3) & 1, (c >> 1) & 3, c & 1
+        if bits == 4:
+            word, p = 2 * i + (kk >> 1), 2 * (kk & 1) + bi
+            return word * 32 + 16 * ln + 4 * (p & 1) + 8 * (p >> 1)
+        word, p = i, 2 * kk + bi
+        return word * 32 + 16 * ln + 2 * (p & 3) + 8 * (p >> 2)
+
+    def rope_bit(c):
+        kk, bi, i, ln = c >> 4, (c >> 3) & 1, (c >> 1) & 3, c & 1
+        return (2 * kk + (i >> 1)) * 32 + 16 * ln + 8 * (i & 1) + 4 * bi
+
+    for bits in (4, 2):
+        cells = sorted(content_bit(c, bits) // bits for c in range(64))
+        assert cells == list(range(64))
+        assert all(content_bit(c, bits) % bits == 0 for c in range(64))
+    assert sorted(rope_bit(c) // 4 for c in range(64)) == list(range(64))

@@ -1,0 +1,174 @@
+"""GPU parity of libmlaq against the CPU oracle (codes bit-exact, outputs
+within the stated tolerances), called through the C ABI."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+from mlaq_testlib import Case, assert_close_out, expected_codes
+
+pytestmark = pytest.mark.gpu
+
+EDGE_LENS = [0, 1, 3, 4, 5, 63, 64, 65, 131, 132, 133, 200, 257, 1000, 4097]
+
+
+def _export_all(case):
+    bs, ts = [], []
+    for b, L in enumerate(case.seq_lens):
+        bs += [b] * L
+        ts += list(range(L))
+    tb = torch.tensor(bs, dtype=torch.int32, device="cuda")
+    tt = torch.tensor(ts, dtype=torch.int32, device="cuda")
+    codes, meta = case.cache.export_tokens(case.pt_d, tb, tt)
+    return codes.cpu().numpy(), meta.cpu().numpy()
+
+
+@pytest.mark.parametrize("mode", ["C4R4", "C2R4"])
+def test_writer_codes_meta_ring_bit_exact(mode):
+    case = Case(mode, EDGE_LENS, 16, seed=11)
+    case.build()
+    assert case.cache.device_status() == 0
+    assert case.seq_d.cpu().tolist() == case.seq_lens
+    codes, meta = _export_all(case)
+    off = 0
+    ring = case.cache.ring_view().float().cpu().numpy()
+    for b, L in enumerate(case.seq_lens):
+        if L == 0:
+            continue
+        ec, em = expected_codes(case, b)
+        np.testing.assert_array_equal(codes[off:off + L], ec, err_msg=f"codes seq {b} L={L}")
+        np.testing.assert_array_equal(meta[off:off + L].view(np.uint16), em.view(np.uint16),
+                                      err_msg=f"meta seq {b} L={L}")
+        off += L
+        er, valid = O.expected_ring(case.tokens(b), L)
+        np.testing.assert_array_equal(ring[b][valid], er[valid], err_msg=f"ring seq {b} L={L}")
+
+
+def test_writer_bf16_pages_hold_tokens():
+    case = Case("BF16", [1, 64, 65, 300], 16, seed=12)
+    case.build()
+    pages = case.cache.codes.view(torch.bfloat16).view(-1, 64, 576).cpu()
+    for b, L in enumerate(case.seq_lens):
+        tok = torch.from_numpy(case.tokens(b))
+        for t in range(L):
+            p = int(case.page_table[b, t // 64])
+            assert torch.equal(pages[p, t % 64].float(), tok[t]), (b, t)
+
+
+@pytest.mark.parametrize("mode", ["C4R4", "C2R4", "BF16"])
+def test_decode_tiny_workload(mode):
+    wl = W.workload("tiny_c4r4")
+    case = Case(mode, wl.seq_lens, wl.H, seed=wl.seed)
+    case.build()
+    out, lse = case.decode()
+    for b in range(case.B):
+        ro, rl = case.oracle_seq(b)
+        assert_close_out(out[b], lse[b], ro, rl, f"{mode} seq {b}")
+    assert case.cache.device_status() == 0
+
+
+@pytest.mark.parametrize("mode", ["C4R4", "C2R4", "BF16"])
+def test_decode_edge_lengths(mode):
+    case = Case(mode, EDGE_LENS, 16, seed=13)
+    case.build()
+    out, lse = case.decode()
+    for b, L in enumerate(case.seq_lens):
+        ro, rl = case.oracle_seq(b)
+        assert_close_out(out[b], lse[b], ro, rl, f"{mode} L={L}")
+
+
+@pytest.mark.parametrize("H", [32, 128])
+def test_decode_more_heads(H):
+    case = Case("C4R4", [5, 140, 777, 2048], H, seed=14)
+    case.build()
+    out, lse = case.decode()
+    for b in range(case.B):
+        ro, rl = case.oracle_seq(b)
+        assert_close_out(out[b], lse[b], ro, rl, f"H={H} seq {b}")
+
+
+def test_split_invariance():
+    case = Case("C4R4", [3000, 9000, 133, 640], 16, seed=15)
+    case.build()
+    case.cache.set_decode_ctas(1)
+    o1, l1 = case.decode()
+    o1, l1 = o1.clone(), l1.clone()
+    case.cache.set_decode_ctas(600)
+    o2, l2 = case.decode()
+    for b in range(case.B):
+        ro, rl = case.oracle_seq(b)
+        assert_close_out(o1[b], l1[b], ro, rl, f"1 split seq {b}")
+        assert_close_out(o2[b], l2[b], ro, rl, f"many splits seq {b}")
+    assert torch.allclose(l1, l2, atol=1e-4)
+
+
+def test_incremental_append_retires_without_requant():
+    # Append one token per step across the sink/recent boundary; every
+    # token's stored codes equal the bulk quantization (no re-quantization),
+    # and decode matches the oracle at several lengths.
+    L0 = [100, 130, 2000]
+    steps = 40
+    case = Case("C4R4", [L + steps for L in L0], 16, seed=16)
+    from bit_mla_kv_gb300.mlaq import Cache
+    cache = Cache("C4R4", case.num_pages, case.B, case.page_table.shape[1], max_heads=16)
+    case.cache = cache
+    case.pt_d = case.page_table.cuda()
+    case.seq_d = torch.zeros(case.B, dtype=torch.int32, device="cuda")
+    # prefill the first L0 tokens of each sequence
+    cu0 = torch.zeros(case.B + 1, dtype=torch.int32)
+    cu0[1:] = torch.cumsum(torch.tensor(L0), 0)
+    rows = torch.cat([torch.arange(int(case.cu[b]), int(case.cu[b]) + L0[b]) for b in range(case.B)])
+    cache.append(case.pt_d, case.seq_d, case.c[rows].cuda().contiguous(), case.k[rows].cuda().contiguous(),
+                 cu_new=cu0.cuda())
+    for s in range(steps):
+        rows = torch.tensor([int(case.cu[b]) + L0[b] + s for b in range(case.B)])
+        cache.append(case.pt_d, case.seq_d, case.c[rows].view(case.B, 1, 512).cuda().contiguous(),
+                     case.k[rows].view(case.B, 1, 64).cuda().contiguous())
+        if s in (0, 2, 31, 39):
+            out, lse = case.decode()
+            for b in range(case.B):
+                ro, rl = case.oracle_seq(b, L=L0[b] + s + 1)
+                assert_close_out(out[b], lse[b], ro, rl, f"step {s} seq {b}")
+    assert case.seq_d.cpu().tolist() == case.seq_lens
+    codes, meta = _export_all(case)
+    off = 0
+    for b, L in enumerate(case.seq_lens):
+        ec, em = expected_codes(case, b)
+        np.testing.assert_array_equal(codes[off:off + L], ec)
+        np.testing.assert_array_equal(meta[off:off + L].view(np.uint16), em.view(np.uint16))
+        off += L
+
+
+def test_device_status_reports_bad_page_without_fault():
+    case = Case("C4R4", [500, 700], 16, seed=17)
+    case.build()
+    bad = case.page_table.clone()
+    bad[1, 3] = case.num_pages + 5   # outside the pool: masked out by the kernel's bounds check
+    out, lse = case.cache.decode(case.ql.cuda(), case.qr.cuda(), bad.cuda(), case.seq_d, case.scale)
+    st = case.cache.device_status()
+    assert st & 0x1
+    ro, rl = case.oracle_seq(0)
+    assert_close_out(out[0], lse[0], ro, rl, "untouched sequence")
+    assert torch.isfinite(out[1].float()).all()
+    case.cache.clear_status()
+    assert case.cache.device_status() == 0
+
+
+@pytest.mark.parametrize("name,sample", [("v2lite_c4r4", [0, 7, 19, 31]), ("v3_c4r4", [0, 63]),
+                                         ("long_c2r4", [2]), ("long_c4r4", [1]), ("long_bf16", [3])])
+def test_full_size_sampled(name, sample):
+    """Full workload sizes in the benchmark's launch configuration; the oracle
+    checks whole sampled sequences."""
+    wl = W.workload(name)
+    case = Case(wl.mode, wl.seq_lens, wl.H, seed=wl.seed, gen_device="cuda")
+    case.build()
+    out, lse = case.decode()
+    assert case.cache.device_status() == 0
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    for b in sample:
+        ro, rl = case.oracle_seq(b)
+        assert_close_out(out[b], lse[b], ro, rl, f"{name} seq {b}")
