@@ -33,7 +33,8 @@ int mlaq_buffer_sizes(int mode, int32_t num_pages, int32_t max_seqs, int32_t max
                       size_t* meta_bytes, size_t* ring_bytes, size_t* workspace_bytes) {
   if (!valid_mode(mode)) return MLAQ_ERR_MODE;
   if (!codes_bytes || !meta_bytes || !ring_bytes || !workspace_bytes) return MLAQ_ERR_NULL;
-  if (num_pages <= 0 || max_seqs <= 0 || max_heads < 16 || max_heads > 128 || max_heads % 16) return MLAQ_ERR_SHAPE;
+  if (num_pages <= 0 || max_seqs <= 0 || max_seqs > kMaxSeqs || max_heads < 16 || max_heads > 128 || max_heads % 16)
+    return MLAQ_ERR_SHAPE;
   *codes_bytes = (size_t)num_pages * page_code_bytes(mode);
   *meta_bytes = mode == MLAQ_BF16 ? 0 : (size_t)num_pages * kMetaPage;
   *ring_bytes = mode == MLAQ_BF16 ? 0 : (size_t)max_seqs * kRing * kD * 2;
@@ -47,8 +48,8 @@ int mlaq_cache_create(mlaq_cache** out, int mode, int32_t num_pages, int32_t max
   if (!out) return MLAQ_ERR_NULL;
   *out = nullptr;
   if (!valid_mode(mode)) return MLAQ_ERR_MODE;
-  if (num_pages <= 0 || max_seqs <= 0 || max_pages_per_seq <= 0 || max_heads < 16 || max_heads > 128 ||
-      max_heads % 16)
+  if (num_pages <= 0 || max_seqs <= 0 || max_seqs > kMaxSeqs || max_pages_per_seq <= 0 || max_heads < 16 ||
+      max_heads > 128 || max_heads % 16)
     return MLAQ_ERR_SHAPE;
   if (!codes || !workspace || (mode != MLAQ_BF16 && (!meta || !ring))) return MLAQ_ERR_NULL;
   if (!aligned16(codes) || !aligned16(workspace) || (mode != MLAQ_BF16 && (!aligned16(meta) || !aligned16(ring))))

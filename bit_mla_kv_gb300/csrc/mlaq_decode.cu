@@ -269,12 +269,13 @@ template <int MODE>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
-  const int item_idx = blockIdx.x;
+  // head blocks of one item are adjacent in launch order so they share L2
+  const int item_idx = blockIdx.y;
   if (item_idx >= *p.num_items) return;
   const Item it = p.items[item_idx];
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int r = lane >> 2, i = lane & 3;
-  const int h0 = blockIdx.y * 16;
+  const int h0 = blockIdx.x * 16;
   const int nst = StagePlan<MODE>::count(it);
   constexpr int CB = token_bytes(MODE);
   constexpr int CBITS = content_bits(MODE);
@@ -702,7 +703,7 @@ static cudaError_t run_decode(mlaq_cache* c, const DecodeParams& p, int grid_x, 
     ev = reinterpret_cast<cudaEvent_t*>(c->timing_events) + 2 * c->timing_n;
     cudaEventRecord(ev[0], s);
   }
-  decode_kernel<MODE><<<dim3(grid_x, grid_y), kThreads, smem, s>>>(p);
+  decode_kernel<MODE><<<dim3(grid_y, grid_x), kThreads, smem, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (ev) {
     cudaEventRecord(ev[1], s);

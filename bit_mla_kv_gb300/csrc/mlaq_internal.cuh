@@ -27,6 +27,7 @@ constexpr size_t kWsStatus = 0;          // int32 sticky status
 constexpr size_t kWsNumItems = 4;        // int32 number of work items of the last plan
 constexpr size_t kWsItems = 256;         // int4 items[max_items]
 constexpr int kMaxPlanCtas = 1024;       // decode CTA target never exceeds this
+constexpr int kMaxSeqs = 16384;          // work items index gridDim.y (< 65536)
 
 __host__ __device__ constexpr int content_bits(int mode) { return mode == MLAQ_C2R4 ? 2 : 4; }
 // Bytes of codes per token in a page (BF16 mode: the raw token).

@@ -90,6 +90,7 @@ typedef enum mlaq_status {
  *              slot (0 for BF16);
  *   workspace: split-KV plan, partial outputs and the device status word,
  *              for batches up to max_seqs sequences and max_heads heads.
+ * Limits: 1 <= max_seqs <= 16384; max_heads a multiple of 16 in [16, 128].
  * Returns MLAQ_ERR_SHAPE / MLAQ_ERR_MODE for bad sizes. Host only. */
 int mlaq_buffer_sizes(int mode, int32_t num_pages, int32_t max_seqs, int32_t max_heads,
                       size_t* codes_bytes, size_t* meta_bytes, size_t* ring_bytes,
