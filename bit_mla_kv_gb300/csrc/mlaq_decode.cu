@@ -41,6 +41,7 @@ constexpr int kSpStride = 20;                      // floats per row of partial 
 constexpr int kPStride = 24;                       // halfs per row of P [h][t]
 constexpr int kMinPagesPerSplit = 4;
 constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr int kMaxDevices = 64;
 
 struct DecodeParams {
   const uint8_t* codes;
@@ -377,8 +378,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
     for (int s = 0; s < nsteps; ++s) {
       const int tb = base + s * kT;
       const int lr = s * kT + r;  // local row of token r in the stage
-      const bool v0 = ok && !bad && token_valid(it, tb + r);
-      const bool v1 = ok && !bad && token_valid(it, tb + 8 + r);
+      // every token of the step valid (the common case inside a packed range)
+      const bool all_in = it.kind == 0 && tb >= it.tlo && tb + kT <= it.thi;
+      const bool v0 = ok && !bad && (all_in || token_valid(it, tb + r));
+      const bool v1 = ok && !bad && (all_in || token_valid(it, tb + 8 + r));
       // ---------------- dequant + scores
       // meta for tokens r (x) and r+8 (y), groups j = 0, 1 (content), 2 (rope)
       uint32_t mx[3], my[3];
@@ -545,8 +548,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
           x0 += v.x;
           x1 += v.y;
         }
-        const bool ok0 = !bad && token_valid(it, tb + tp);
-        const bool ok1 = !bad && token_valid(it, tb + tp + 1);
+        const bool ok0 = !bad && (all_in || token_valid(it, tb + tp));
+        const bool ok1 = !bad && (all_in || token_valid(it, tb + tp + 1));
         x0 = ok0 ? x0 * p.scale_log2 : -INFINITY;
         x1 = ok1 ? x1 * p.scale_log2 : -INFINITY;
         float tmax = fmaxf(x0, x1);
@@ -696,8 +699,17 @@ __global__ void combine_kernel(const float* o_part, const float* lse_part, const
 template <int MODE>
 static cudaError_t run_decode(mlaq_cache* c, const DecodeParams& p, int grid_x, int grid_y, cudaStream_t s) {
   const int smem = (int)sizeof(DecodeSmem);
-  cudaError_t ea = cudaFuncSetAttribute(decode_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // Opt in to >48 KB of dynamic shared memory once per device (the first call
+  // on a device must not be inside a stream capture).
+  static bool attr_done[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t ea = cudaGetDevice(&dev);
   if (ea != cudaSuccess) return ea;
+  if (dev < 0 || dev >= kMaxDevices || !attr_done[dev]) {
+    ea = cudaFuncSetAttribute(decode_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (ea != cudaSuccess) return ea;
+    if (dev >= 0 && dev < kMaxDevices) attr_done[dev] = true;
+  }
   cudaEvent_t* ev = nullptr;
   if (c->timing_events && c->timing_n < c->timing_max) {
     ev = reinterpret_cast<cudaEvent_t*>(c->timing_events) + 2 * c->timing_n;

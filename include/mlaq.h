@@ -144,7 +144,9 @@ int mlaq_append(mlaq_cache* cache, const int32_t* page_table, int32_t* seq_lens,
  * Work is split over the GPU (split-KV) by a device-side planner from
  * seq_lens, and merged by a log-sum-exp combine kernel: three launches, no
  * host sync. Inputs must lie in fp16 range (|x| < 65504; the kernel computes
- * in fp16 operands with fp32 accumulation).
+ * in fp16 operands with fp32 accumulation). The first call on a device opts
+ * the attention kernel into large shared memory (a host-side attribute), so
+ * make that first call outside any CUDA-graph capture; later calls capture.
  */
 int mlaq_decode(mlaq_cache* cache, const uint16_t* q_latent, const uint16_t* q_rope,
                 const int32_t* page_table, const int32_t* seq_lens, int32_t B, int32_t H,

@@ -172,3 +172,88 @@ def test_full_size_sampled(name, sample):
     for b in sample:
         ro, rl = case.oracle_seq(b)
         assert_close_out(out[b], lse[b], ro, rl, f"{name} seq {b}")
+
+
+def test_serving_loop_sampled():
+    """Serving loop at full size: B=128, H=16, L0~U[2K,16K], 256 steps of
+    mlaq_append (one token per sequence) + mlaq_decode. Appended codes are
+    checked bit-exactly at steps {0,1,127,128,255}; decode outputs of sampled
+    sequences at steps {0,128,255} against the oracle."""
+    wl = W.workload("serving_c4r4")
+    steps = wl.steps
+    final = [L + steps for L in wl.seq_lens]
+    case = Case("C4R4", final, wl.H, seed=wl.seed, gen_device="cuda")
+    from bit_mla_kv_gb300.mlaq import Cache
+    cache = Cache("C4R4", case.num_pages, case.B, case.page_table.shape[1], max_heads=16)
+    case.cache = cache
+    case.pt_d = case.page_table.cuda()
+    case.seq_d = torch.zeros(case.B, dtype=torch.int32, device="cuda")
+    cu = case.cu.long()
+    first = torch.cat([torch.arange(int(cu[b]), int(cu[b]) + wl.seq_lens[b]) for b in range(case.B)]).cuda()
+    cu0 = torch.zeros(case.B + 1, dtype=torch.int32)
+    cu0[1:] = torch.cumsum(torch.tensor(wl.seq_lens), 0)
+    cache.append(case.pt_d, case.seq_d, case.c[first].contiguous(), case.k[first].contiguous(), cu_new=cu0.cuda())
+    sample_b = [0, 37, 127]
+    for s in range(steps):
+        rows = torch.tensor([int(cu[b]) + wl.seq_lens[b] + s for b in range(case.B)], device="cuda")
+        cache.append(case.pt_d, case.seq_d, case.c[rows].view(case.B, 1, 512).contiguous(),
+                     case.k[rows].view(case.B, 1, 64).contiguous())
+        if s in (0, 1, 127, 128, 255):
+            tb = torch.arange(case.B, dtype=torch.int32, device="cuda")
+            tt = torch.tensor([wl.seq_lens[b] + s for b in range(case.B)], dtype=torch.int32, device="cuda")
+            codes, meta = cache.export_tokens(case.pt_d, tb, tt)
+            tok = torch.cat([case.c[rows], case.k[rows]], -1).float().cpu().numpy()
+            ec, em = O.quantize_tokens(tok[:, :512], tok[:, 512:], "C4R4")
+            np.testing.assert_array_equal(codes.cpu().numpy(), ec, err_msg=f"step {s}")
+            np.testing.assert_array_equal(meta.cpu().numpy().view(np.uint16), em.view(np.uint16))
+        if s in (0, 128, 255):
+            out, lse = case.decode()
+            for b in sample_b:
+                ro, rl = case.oracle_seq(b, L=wl.seq_lens[b] + s + 1)
+                assert_close_out(out[b], lse[b], ro, rl, f"step {s} seq {b}")
+    assert case.seq_d.cpu().tolist() == final
+    assert cache.device_status() == 0
+
+
+def test_cuda_graph_capture_of_append_decode():
+    """One serving step (append + decode) captured in a CUDA graph and replayed
+    gives the same results as eager execution."""
+    case = Case("C4R4", [700, 1500, 3000], 16, seed=18, extra_capacity=64)
+    case.build()
+    dev = "cuda"
+    ql, qr = case.ql.to(dev).contiguous(), case.qr.to(dev).contiguous()
+    g = W.generator(99, dev)
+    newc, newk = W.make_tokens(case.B * 8, case.stats, g, dev)
+    newc, newk = newc.view(8, case.B, 1, 512), newk.view(8, case.B, 1, 64)
+    # eager reference on a copy of the cache state
+    ref_cache = Case("C4R4", [700, 1500, 3000], 16, seed=18, extra_capacity=64)
+    ref_cache.build()
+    outs_ref = []
+    for s in range(8):
+        ref_cache.cache.append(ref_cache.pt_d, ref_cache.seq_d, newc[s].contiguous(), newk[s].contiguous())
+        o, l = ref_cache.cache.decode(ql, qr, ref_cache.pt_d, ref_cache.seq_d, case.scale)
+        outs_ref.append((o.clone(), l.clone()))
+    # graph: static input buffers
+    bc = torch.empty_like(newc[0])
+    bk = torch.empty_like(newk[0])
+    out = torch.empty(case.B, 16, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(case.B, 16, dtype=torch.float32, device=dev)
+    # warm the attribute setting outside capture
+    s0 = torch.cuda.Stream()
+    s0.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s0):
+        case.cache.decode(ql, qr, case.pt_d, case.seq_d, case.scale, out=out, lse=lse)
+    torch.cuda.current_stream().wait_stream(s0)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        case.cache.append(case.pt_d, case.seq_d, bc, bk)
+        case.cache.decode(ql, qr, case.pt_d, case.seq_d, case.scale, out=out, lse=lse)
+    for s in range(8):
+        bc.copy_(newc[s])
+        bk.copy_(newk[s])
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, outs_ref[s][0]), s
+        assert torch.equal(lse, outs_ref[s][1]), s
+    assert case.seq_d.cpu().tolist() == ref_cache.seq_d.cpu().tolist()
