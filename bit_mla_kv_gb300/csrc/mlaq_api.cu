@@ -6,6 +6,10 @@
 
 namespace mlaq {
 size_t workspace_bytes_for(int max_seqs, int max_heads);
+int launch_decode_static(int mode, const void* codes, const void* meta, const void* ring, int num_pages,
+                         int max_pages_per_seq, const uint16_t* q_latent, const uint16_t* q_rope,
+                         const int32_t* page_table, const int32_t* seq_lens, int B, int H, float scale,
+                         uint16_t* out, float* lse, int32_t* dev_status, cudaStream_t s);
 }
 
 using namespace mlaq;
@@ -117,6 +121,24 @@ int mlaq_decode(mlaq_cache* c, const uint16_t* q_latent, const uint16_t* q_rope,
   cudaError_t e = launch_decode(c, q_latent, q_rope, page_table, seq_lens, B, H, softmax_scale, out_latent, lse,
                                 reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLAQ_OK : MLAQ_ERR_CUDA;
+}
+
+int mlaq_decode_noalloc(int mode, const void* codes, const void* meta, const void* ring, int32_t num_pages,
+                        int32_t max_pages_per_seq, const uint16_t* q_latent, const uint16_t* q_rope,
+                        const int32_t* page_table, const int32_t* seq_lens, int32_t B, int32_t H,
+                        float softmax_scale, uint16_t* out_latent, float* lse, int32_t* dev_status,
+                        struct CUstream_st* stream) {
+  if (!valid_mode(mode)) return MLAQ_ERR_MODE;
+  if (!codes || !q_latent || !q_rope || !page_table || !seq_lens || !out_latent || !lse) return MLAQ_ERR_NULL;
+  if (mode != MLAQ_BF16 && (!meta || !ring)) return MLAQ_ERR_NULL;
+  if (num_pages <= 0 || max_pages_per_seq <= 0) return MLAQ_ERR_SHAPE;
+  if (B <= 0 || B > kMaxSeqs || H < 16 || H > 128 || H % 16) return MLAQ_ERR_SHAPE;
+  if (!aligned16(codes) || !aligned16(q_latent) || !aligned16(q_rope) || !aligned16(out_latent) ||
+      (mode != MLAQ_BF16 && (!aligned16(meta) || !aligned16(ring))))
+    return MLAQ_ERR_ALIGN;
+  return launch_decode_static(mode, codes, meta, ring, num_pages, max_pages_per_seq, q_latent, q_rope, page_table,
+                              seq_lens, B, H, softmax_scale, out_latent, lse, dev_status,
+                              reinterpret_cast<cudaStream_t>(stream));
 }
 
 int mlaq_export_tokens(mlaq_cache* c, const int32_t* page_table, int32_t B, const int32_t* token_b,

@@ -783,3 +783,74 @@ size_t workspace_bytes_for(int max_seqs, int max_heads) {
 }
 
 }  // namespace mlaq
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode.
+//
+// For callers that cannot allocate device memory themselves: code running
+// inside another runtime's allocator, a plugin that may not call cudaMalloc
+// while a stream is being captured, or a host that pre-reserves all of HBM.
+// The plan and the split partials normally live in the caller's workspace;
+// here they live in a fixed array inside this library. The array is a
+// file-scope __device__ variable, so every GPU that loads the library holds
+// it until the process exits.
+namespace mlaq {
+
+constexpr size_t kStaticScratchBytes = (size_t)64 << 20;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+static void* g_static_ptr[kMaxDevices];
+static int g_static_sms[kMaxDevices];
+
+// Once per device, with that device current: the scratch array's device
+// address (host code only sees a host-side stand-in for the symbol) and the
+// SM count the planner sizes the grid for.
+static cudaError_t static_scratch_setup(int dev) {
+  if (g_static_ptr[dev]) return cudaSuccess;
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+  if (e != cudaSuccess) return e;
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  g_static_sms[dev] = sms;
+  g_static_ptr[dev] = p;
+  return cudaSuccess;
+}
+
+size_t static_scratch_bytes() { return kStaticScratchBytes; }
+
+// Returns MLAQ_* status (argument errors) or MLAQ_ERR_CUDA.
+int launch_decode_static(int mode, const void* codes, const void* meta, const void* ring, int num_pages,
+                         int max_pages_per_seq, const uint16_t* q_latent, const uint16_t* q_rope,
+                         const int32_t* page_table, const int32_t* seq_lens, int B, int H, float scale,
+                         uint16_t* out, float* lse, int32_t* dev_status, cudaStream_t s) {
+  if (workspace_bytes_for(B, H) > kStaticScratchBytes) return MLAQ_ERR_CAPACITY;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLAQ_ERR_CUDA;
+  if (static_scratch_setup(dev) != cudaSuccess) return MLAQ_ERR_CUDA;
+  mlaq_cache c = {};
+  c.mode = mode;
+  c.num_pages = num_pages;
+  c.max_seqs = B;
+  c.max_pages_per_seq = max_pages_per_seq;
+  c.max_heads = H;
+  c.codes = const_cast<void*>(codes);
+  c.meta = const_cast<void*>(meta);
+  c.ring = const_cast<void*>(ring);
+  c.workspace = g_static_ptr[dev];
+  c.workspace_bytes = kStaticScratchBytes;
+  c.num_sms = g_static_sms[dev];
+  c.decode_ctas = 2 * c.num_sms < kMaxPlanCtas ? 2 * c.num_sms : kMaxPlanCtas;
+  char* ws = static_cast<char*>(c.workspace);
+  // the status word is sticky: start each call from zero
+  if (cudaMemsetAsync(ws + kWsStatus, 0, sizeof(int), s) != cudaSuccess) return MLAQ_ERR_CUDA;
+  if (launch_decode(&c, q_latent, q_rope, page_table, seq_lens, B, H, scale, out, lse, s) != cudaSuccess)
+    return MLAQ_ERR_CUDA;
+  if (dev_status &&
+      cudaMemcpyAsync(dev_status, ws + kWsStatus, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return MLAQ_ERR_CUDA;
+  return MLAQ_OK;
+}
+
+}  // namespace mlaq

@@ -34,6 +34,7 @@ EXPORTED = [
     "mlaq_buffer_sizes", "mlaq_cache_create", "mlaq_cache_destroy", "mlaq_append", "mlaq_decode",
     "mlaq_export_tokens", "mlaq_cache_bytes", "mlaq_get_device_status", "mlaq_clear_device_status",
     "mlaq_timing_enable", "mlaq_timing_read", "mlaq_set_decode_ctas", "mlaq_status_string",
+    "mlaq_decode_noalloc",
 ]
 
 _lib.mlaq_status_string.restype = ctypes.c_char_p
@@ -51,6 +52,8 @@ _lib.mlaq_clear_device_status.argtypes = [_vp, _vp]
 _lib.mlaq_timing_enable.argtypes = [_vp, _i32]
 _lib.mlaq_timing_read.argtypes = [_vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(_i32)]
 _lib.mlaq_set_decode_ctas.argtypes = [_vp, _i32]
+_lib.mlaq_decode_noalloc.argtypes = [ctypes.c_int, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _i32,
+                                     ctypes.c_float, _vp, _vp, _vp, _vp]
 for _name in EXPORTED:
     if _name != "mlaq_status_string":
         getattr(_lib, _name).restype = ctypes.c_int
@@ -208,6 +211,25 @@ class Cache:
         n = ctypes.c_int32()
         _check(_lib.mlaq_timing_read(self._h, buf, ctypes.byref(n)), "mlaq_timing_read")
         return [buf[k] for k in range(n.value)]
+
+    def decode_noalloc(self, q_latent, q_rope, page_table, seq_lens, softmax_scale, out=None, lse=None,
+                       dev_status=None, stream=None):
+        """mlaq_decode_noalloc over this cache's pools: the split-KV scratch
+        comes from the library's fixed device array instead of the workspace."""
+        B, H = q_latent.shape[0], q_latent.shape[1]
+        _need(q_latent, torch.bfloat16, (B, H, 512), "q_latent")
+        _need(q_rope, torch.bfloat16, (B, H, 64), "q_rope")
+        _need(page_table, torch.int32, (B, self.max_pages_per_seq), "page_table")
+        _need(seq_lens, torch.int32, (B,), "seq_lens")
+        if out is None:
+            out = torch.empty(B, H, 512, dtype=torch.bfloat16, device=q_latent.device)
+        if lse is None:
+            lse = torch.empty(B, H, dtype=torch.float32, device=q_latent.device)
+        _check(_lib.mlaq_decode_noalloc(MODES[self.mode], _ptr(self.codes), _ptr(self.meta), _ptr(self.ring),
+                                        self.num_pages, self.max_pages_per_seq, _ptr(q_latent), _ptr(q_rope),
+                                        _ptr(page_table), _ptr(seq_lens), B, H, float(softmax_scale), _ptr(out),
+                                        _ptr(lse), _ptr(dev_status), _stream(stream)), "mlaq_decode_noalloc")
+        return out, lse
 
     def set_decode_ctas(self, ctas: int):
         _check(_lib.mlaq_set_decode_ctas(self._h, ctas), "mlaq_set_decode_ctas")

@@ -153,6 +153,35 @@ int mlaq_decode(mlaq_cache* cache, const uint16_t* q_latent, const uint16_t* q_r
                 float softmax_scale, uint16_t* out_latent, float* lse,
                 struct CUstream_st* stream);
 
+/* Allocation-free variant of mlaq_decode. The pages describe no such call;
+ * it exists for callers that cannot allocate device memory: code running
+ * inside another runtime's allocator, plugins that may not call cudaMalloc
+ * while a stream is being captured, or hosts that reserve all of HBM up
+ * front. Such a caller still owns and passes the cache pools (codes, meta,
+ * ring, filled by mlaq_append or an equivalent writer of the same layout),
+ * the inputs and the outputs; only the split-KV scratch (plan, partial
+ * outputs, status word) moves into a fixed 64 MiB array inside this library,
+ * which every GPU that loads the library holds until the process exits.
+ *   mode, num_pages, max_pages_per_seq: describe the pools as for
+ *       mlaq_cache_create (ring holds at least B sequence slots);
+ *   remaining arguments as for mlaq_decode;
+ *   dev_status: optional device int32 that receives this call's device
+ *       status bits (MLAQ_DEV_*), or NULL.
+ * Calls nothing that allocates (no cudaMalloc / cudaFree, no allocating
+ * library routine). Returns MLAQ_ERR_CAPACITY when the scratch needed for
+ * (B, H) exceeds 64 MiB (about B * H <= 8192, e.g. B = 64 at H = 128 or
+ * B = 512 at H = 16). The first call on each device looks up the array's
+ * device address and sets a kernel attribute; make that first call before
+ * any stream capture. Every call uses the same array and the next call
+ * overwrites it (the status word is cleared at the start of each call), so
+ * calls that can overlap on the GPU -- on different streams, or on two
+ * threads -- race and give wrong results; serialise them on one stream. */
+int mlaq_decode_noalloc(int mode, const void* codes, const void* meta, const void* ring,
+                        int32_t num_pages, int32_t max_pages_per_seq, const uint16_t* q_latent,
+                        const uint16_t* q_rope, const int32_t* page_table, const int32_t* seq_lens,
+                        int32_t B, int32_t H, float softmax_scale, uint16_t* out_latent, float* lse,
+                        int32_t* dev_status, struct CUstream_st* stream);
+
 /* Debug / test read-back of n stored tokens in a canonical form independent
  * of the physical packing: for k < n, token token_t[k] of sequence
  * token_b[k] ->
