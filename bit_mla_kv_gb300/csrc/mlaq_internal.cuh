@@ -25,9 +25,9 @@ constexpr int kMetaPage = kPage * kMetaTok;  // 2304
 // Workspace layout (bytes from the workspace base).
 constexpr size_t kWsStatus = 0;          // int32 sticky status
 constexpr size_t kWsNumItems = 4;        // int32 number of work items of the last plan
-constexpr size_t kWsItems = 256;         // int4 items[max_items]
-constexpr int kMaxPlanCtas = 1024;       // decode CTA target never exceeds this
-constexpr int kMaxSeqs = 16384;          // work items index gridDim.y (< 65536)
+constexpr int kMaxPlanCtas = 1024;       // decode CTA count never exceeds this
+constexpr int kMaxSeqs = 16384;          // sequences per call
+constexpr int kMaxHeadBlocks = 8;        // 128 heads / 16
 
 __host__ __device__ constexpr int content_bits(int mode) { return mode == MLAQ_C2R4 ? 2 : 4; }
 // Bytes of codes per token in a page (BF16 mode: the raw token).
@@ -37,17 +37,41 @@ __host__ __device__ constexpr int token_bytes(int mode) {
 __host__ __device__ constexpr int group_code_bytes(int bits) { return kGroup * bits / 8; }
 __host__ __device__ constexpr int page_code_bytes(int mode) { return kPage * token_bytes(mode); }
 
-inline size_t max_items_for(int max_seqs) { return (size_t)2 * max_seqs + kMaxPlanCtas; }
-// Rows (item, head) of the partial outputs: items * H <= 2 B H + 16 * ctas.
+// A work item of the split-KV decode: units [u_lo, u_hi) of sequence b,
+// processed by CTA `cta`. A sequence's units are its ring chunks (16 BF16
+// sink/recent slots each; packed modes) followed by its packed pages (4 units
+// = 4 steps of 16 tokens each) or, in BF16 mode, 16-token quarter pages.
+struct Item {
+  int b, u_lo, u_hi, cta;
+};
+
+// Items: at most one per sequence plus one per CTA boundary inside a sequence.
+inline size_t max_items_for(int max_seqs) { return (size_t)max_seqs + kMaxPlanCtas + 1; }
+// Rows (item, head) of the partial outputs: items * H <= B H + 16 * ctas.
 inline size_t max_partial_rows(int max_seqs, int max_heads) {
-  return (size_t)2 * max_seqs * max_heads + (size_t)16 * kMaxPlanCtas;
+  return (size_t)max_seqs * max_heads + (size_t)16 * kMaxPlanCtas + max_heads;
 }
 
-// Work item of the split-KV decode: sequence b, kind (0 = packed / paged range
-// [tlo, thi), 1 = the sequence's BF16 sink + recent ring).
-struct Item {
-  int b, kind, tlo, thi;
+struct WsLayout {
+  size_t items, item_start, useq, bnd, nonempty, cta_item_start, counters, lse_part, o_part, total;
 };
+inline WsLayout ws_layout(int max_seqs, int max_heads) {
+  auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+  WsLayout L;
+  size_t off = 256;
+  L.items = off;          off += al(max_items_for(max_seqs) * sizeof(Item));
+  L.item_start = off;     off += al(((size_t)max_seqs + 1) * 4);
+  L.useq = off;           off += al(((size_t)max_seqs + 1) * 4);
+  L.bnd = off;            off += al(((size_t)kMaxPlanCtas + 1) * 4);
+  L.nonempty = off;       off += al(((size_t)kMaxPlanCtas + 2) * 4);
+  L.cta_item_start = off; off += al(((size_t)kMaxPlanCtas + 1) * 4);
+  L.counters = off;       off += al((size_t)max_seqs * kMaxHeadBlocks * 4);
+  const size_t rows = max_partial_rows(max_seqs, max_heads);
+  L.lse_part = off;       off += al(rows * 4);
+  L.o_part = off;         off += rows * kDL * 4;
+  L.total = off;
+  return L;
+}
 
 // ---------------------------------------------------------------------------
 // Physical code layout inside a token's bytes.
