@@ -16,16 +16,22 @@ def nvcc_path() -> str:
 
 
 def build(verbose: bool = False, force: bool = False) -> str:
-    """Compile the CUDA sources into bit_mla_kv_gb300/libmlaq.so; returns its path."""
+    """Compile the CUDA sources into bit_mla_kv_gb300/libmlaq.so; returns its path.
+
+    Extra nvcc flags (e.g. -DMLAQ_CTAS_PER_SM=3 -DMLAQ_STAGES=2 for the decode
+    kernel's occupancy and staging depth) may be given in MLAQ_NVCC_FLAGS."""
     srcs = [os.path.join(HERE, "csrc", s) for s in SOURCES]
     deps = srcs + [os.path.join(HERE, "csrc", "mlaq_internal.cuh"),
                    os.path.join(HERE, "..", "include", "mlaq.h")]
+    extra = os.environ.get("MLAQ_NVCC_FLAGS", "").split()
+    if extra:
+        force = True
     if not force and os.path.exists(LIB):
         newest = max(os.path.getmtime(d) for d in deps)
         if os.path.getmtime(LIB) >= newest:
             return LIB
     cmd = [nvcc_path(), "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
-           "-Xcompiler", "-fPIC", "-shared", "-o", LIB + ".tmp"] + srcs
+           "-Xcompiler", "-fPIC", "-shared", "-o", LIB + ".tmp"] + extra + srcs
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     proc = subprocess.run(cmd, capture_output=True, text=True)

@@ -75,7 +75,7 @@ int mlaq_cache_create(mlaq_cache** out, int mode, int32_t num_pages, int32_t max
   c->workspace = workspace;
   c->workspace_bytes = workspace_bytes;
   c->num_sms = sms;
-  c->decode_ctas = 2 * sms < kMaxPlanCtas ? 2 * sms : kMaxPlanCtas;
+  c->decode_ctas = MLAQ_CTAS_PER_SM * sms < kMaxPlanCtas ? MLAQ_CTAS_PER_SM * sms : kMaxPlanCtas;
   *out = c;
   return MLAQ_OK;
 }

@@ -41,14 +41,21 @@ namespace mlaq {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kStages = 4;
+constexpr int kStages = MLAQ_STAGES;
 constexpr int kT = 16;                                // tokens per step
 constexpr int kRingChunks = (kRing + kT - 1) / kT;    // 9
 constexpr int kStageBytes = kPage * 288 + kMetaPage;  // 20736: max(C4R4 page + meta, 16 BF16 tokens)
 constexpr int kSpStride = 20;                         // floats per row of partial scores [h][t]
 constexpr int kPStride = 24;                          // halfs per row of P [h][t]
-constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint64_t kWaitLimit = 200000000ull;  // 200 ms per bounded wait
 constexpr int kMaxDevices = 64;
+#ifndef MLAQ_TC_AGG
+#define MLAQ_TC_AGG 0
+#endif
+// Aggregation on tcgen05 (MLAQ_TC_AGG): O^T[channel][head] accumulates in TMEM.
+constexpr int kAggBufs = 2;      // A (content) / P^T step buffers in flight
+constexpr int kTmemCols = 128;   // O^T: 4 blocks x 16 heads; A: 2 buffers x 4 blocks x 8 columns
+constexpr int kTmemA = 64;       // first column of the A step buffers
 
 struct DecodeParams {
   const uint8_t* codes;
@@ -81,6 +88,12 @@ struct __align__(16) DecodeSmem {
   int stage_bad[kStages];
   int is_last;
   uint64_t full[kStages];
+#if MLAQ_TC_AGG
+  __align__(128) uint8_t pt[kAggBufs][512];  // P^T B operand: 16 heads x 16 tokens, 8x8 core matrices
+  uint64_t agg_done[kAggBufs];
+  uint32_t tmem_base;
+  int rescale_flag[kWarps];
+#endif
 };
 
 __device__ __forceinline__ int clamp_len(int L, int max_tokens) { return min(max(L, 0), max_tokens); }
@@ -275,14 +288,13 @@ __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t u) {
   return h2_as_u32(__float22half2_rn(f));
 }
 
-// Ring slot validity for a sequence of length L (slot j < 4: sink token j;
-// slot 4 + r: the newest token t < L with t mod 128 == r, if t >= 4).
+// Ring slot validity for a sequence of length L. Slot j < 4 holds sink token
+// j. Slot 4 + r holds the newest token t < L with t mod 128 == r, valid iff
+// t >= 4; in closed form: r < L - 128 (then t >= 128) or 4 <= r < L (t = r).
 __device__ __forceinline__ bool ring_slot_valid(int slot, int L) {
-  if (slot >= kRing || L <= 0) return false;
   if (slot < kSink) return slot < L;
   const int r = slot - kSink;
-  const int t = (L - 1) - (((L - 1 - r) % kRecent + kRecent) % kRecent);
-  return t >= kSink;
+  return slot < kRing && ((r < L - kRecent) || (r >= kSink && r < L));
 }
 
 // Stage k of item `it` (sequence length L):
@@ -311,12 +323,12 @@ __device__ __forceinline__ StageRef item_stage(const Item& it, int L, int k) {
 // Row j of a stage holds a token that attention must see.
 template <int MODE>
 __device__ __forceinline__ bool row_valid(const StageRef& st, int j, int L) {
-  if (st.kind == 0) return ring_slot_valid(kT * st.idx + j, L);
-  if (st.kind == 1) {
-    const int t = kPage * st.idx + j;
-    return t >= kSink && t < L - kRecent;
-  }
-  return kT * st.idx + j < L;
+  const int t16 = kT * st.idx + j;     // ring slot (kind 0) or token (kind 2)
+  const int t64 = kPage * st.idx + j;  // token (kind 1)
+  const bool ring = ring_slot_valid(t16, L);
+  const bool page = (t64 >= kSink) & (t64 < L - kRecent);
+  const bool quarter = t16 < L;
+  return st.kind == 0 ? ring : (st.kind == 1 ? page : quarter);
 }
 
 // Producer: issue the bulk copies of a stage into buffer `buf`.
@@ -379,7 +391,7 @@ __device__ void producer_advance(const DecodeParams& p, DecodeSmem& sm, ProdCurs
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
   const int cta = blockIdx.y;
@@ -397,10 +409,26 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(&sm.full[s], 1);
+#if MLAQ_TC_AGG
+    for (int s = 0; s < kAggBufs; ++s) mbar_init(&sm.agg_done[s], kWarps);
+#endif
     fence_mbar_init();
     fence_proxy_async();
   }
+#if MLAQ_TC_AGG
+  if (w == 0) {
+    tmem_alloc(&sm.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+#endif
   __syncthreads();
+#if MLAQ_TC_AGG
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  int agg_ctr = 0;  // aggregation steps issued by this CTA
+  constexpr uint32_t kAggIdesc = umma_idesc_f16(128, 16);
+#endif
   ProdCursor pc;
   if (tid == 0) {
     const Item it = p.items[i0];
@@ -473,6 +501,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
       }
     }
 
+#if MLAQ_TC_AGG
+    bool item_first = true;  // the item's first aggregation MMA overwrites O^T
+#else
     float o[2][4][2][4];  // O[h = r / r+8][c = 64(2w+j) + 16kk + 8cb + 2i..]
 #pragma unroll
     for (int j = 0; j < 2; ++j)
@@ -482,6 +513,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
         for (int cb = 0; cb < 2; ++cb)
 #pragma unroll
           for (int e = 0; e < 4; ++e) o[j][kk][cb][e] = 0.f;
+#endif
     float m_run = -INFINITY, l_run = 0.f;
 
     const int nst = item_stages<MODE>(it, L);
@@ -501,8 +533,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
           const int t0 = kPage * sref.idx + s * kT;
           all_in = t0 >= kSink && t0 + kT <= L - kRecent;
         }
-        const bool v0 = ok && !bad && (all_in || row_valid<MODE>(sref, lr, L));
-        const bool v1 = ok && !bad && (all_in || row_valid<MODE>(sref, lr + 8, L));
+        const bool live = ok & !bad;
+        const bool v0 = live & (all_in | row_valid<MODE>(sref, lr, L));
+        const bool v1 = live & (all_in | row_valid<MODE>(sref, lr + 8, L));
         // ---------------- dequant + scores
         uint32_t mx[3], my[3];  // meta (s, mn) of tokens r (x) and r+8 (y), groups 2w, 2w+1, rope
         uint32_t ch[2][4][4];   // fp16 A fragments of the content tile (exact codes, later dequantized)
@@ -517,8 +550,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
 #pragma unroll
           for (int j = 0; j < 3; ++j) {
             const int gg = j < 2 ? 2 * w + j : 8;
-            mx[j] = v0 ? *reinterpret_cast<const uint32_t*>(mtab + lr * kMetaTok + 4 * gg) : 0u;
-            my[j] = v1 ? *reinterpret_cast<const uint32_t*>(mtab + (lr + 8) * kMetaTok + 4 * gg) : 0u;
+            const uint32_t mxr = *reinterpret_cast<const uint32_t*>(mtab + lr * kMetaTok + 4 * gg);
+            const uint32_t myr = *reinterpret_cast<const uint32_t*>(mtab + (lr + 8) * kMetaTok + 4 * gg);
+            mx[j] = v0 ? mxr : 0u;
+            my[j] = v1 ? myr : 0u;
           }
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
@@ -599,31 +634,35 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
 #pragma unroll
           for (int hb = 0; hb < 2; ++hb) mma16816(sacc[hb], a, kmn[hb], 0u);
         }
-        // scale terms per group
-#pragma unroll
-        for (int j = 0; j < 3; ++j) {
-          float d[2][4];
+        // scale terms: D_j = codes_j . Q_j per group; the two content-group
+        // chains are interleaved, Q fragments come from the shared table.
+        {
+          float d0[2][4], d1[2][4], d2[2][4];
 #pragma unroll
           for (int hb = 0; hb < 2; ++hb)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) d[hb][e] = 0.f;
-          if (j < 2) {
+            for (int e = 0; e < 4; ++e) d0[hb][e] = d1[hb][e] = d2[hb][e] = 0.f;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-              for (int hb = 0; hb < 2; ++hb) mma16816(d[hb], ch[j][kk], qf[j][kk][hb][0], qf[j][kk][hb][1]);
-          } else {
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb) mma16816(d[hb], rf, qr[hb][0], qr[hb][1]);
+          for (int kk = 0; kk < 4; ++kk) {
+            mma16816(d0[0], ch[0][kk], qf[0][kk][0][0], qf[0][kk][0][1]);
+            mma16816(d1[0], ch[1][kk], qf[1][kk][0][0], qf[1][kk][0][1]);
+            mma16816(d0[1], ch[0][kk], qf[0][kk][1][0], qf[0][kk][1][1]);
+            mma16816(d1[1], ch[1][kk], qf[1][kk][1][0], qf[1][kk][1][1]);
           }
-          const float sx = __half2float(__ushort_as_half((unsigned short)(mx[j] & 0xffffu)));
-          const float sy = __half2float(__ushort_as_half((unsigned short)(my[j] & 0xffffu)));
+          mma16816(d2[0], rf, qr[0][0], qr[0][1]);
+          mma16816(d2[1], rf, qr[1][0], qr[1][1]);
+          float sxv[3], syv[3];
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            sxv[j] = __half2float(__ushort_as_half((unsigned short)(mx[j] & 0xffffu)));
+            syv[j] = __half2float(__ushort_as_half((unsigned short)(my[j] & 0xffffu)));
+          }
 #pragma unroll
           for (int hb = 0; hb < 2; ++hb) {
-            sacc[hb][0] = fmaf(sx, d[hb][0], sacc[hb][0]);
-            sacc[hb][1] = fmaf(sx, d[hb][1], sacc[hb][1]);
-            sacc[hb][2] = fmaf(sy, d[hb][2], sacc[hb][2]);
-            sacc[hb][3] = fmaf(sy, d[hb][3], sacc[hb][3]);
+            sacc[hb][0] = fmaf(sxv[2], d2[hb][0], fmaf(sxv[1], d1[hb][0], fmaf(sxv[0], d0[hb][0], sacc[hb][0])));
+            sacc[hb][1] = fmaf(sxv[2], d2[hb][1], fmaf(sxv[1], d1[hb][1], fmaf(sxv[0], d0[hb][1], sacc[hb][1])));
+            sacc[hb][2] = fmaf(syv[2], d2[hb][2], fmaf(syv[1], d1[hb][2], fmaf(syv[0], d0[hb][2], sacc[hb][2])));
+            sacc[hb][3] = fmaf(syv[2], d2[hb][3], fmaf(syv[1], d1[hb][3], fmaf(syv[0], d0[hb][3], sacc[hb][3])));
           }
         }
         // publish partial scores: sacc[hb] = S[t = r (e 0,1) / r+8 (e 2,3)][h = 8hb + 2i (+1)]
@@ -649,8 +688,29 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
             ch[j][kk][3] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][3]), s2y, m2y)));
           }
         }
+#if MLAQ_TC_AGG
+        // content tile -> TMEM A step buffer (lanes = channels, columns = token pairs)
+        const int ab = agg_ctr % kAggBufs;
+        bool agg_ok = true;
+        if (agg_ctr >= kAggBufs)  // MMAs that last read this buffer must be complete
+          agg_ok = mbar_wait_bounded(&sm.agg_done[ab], ((agg_ctr / kAggBufs) - 1) & 1, kWaitLimit);
+        tc_fence_after();
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const int blk = 2 * j + (kk >> 1);
+            const uint32_t ta = tmem + ((uint32_t)(32 * w + 16 * (kk & 1)) << 16) +
+                                (uint32_t)(kTmemA + 32 * ab + 8 * blk);
+            tmem_st_16x256b(ta, ch[j][kk][0], ch[j][kk][1], ch[j][kk][2], ch[j][kk][3]);
+          }
+        tmem_wait_st();
+        tc_fence_before();
+#else
+        const bool agg_ok = true;
+#endif
         // barrier 1: partial scores complete; also agrees on a timed-out wait
-        if (named_bar_or(1, kThreads, !ok)) {
+        if (named_bar_or(1, kThreads, !(ok && agg_ok))) {
           failed = true;
           g_fail = g - 1;
           break;
@@ -667,26 +727,76 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
             x0 += v.x;
             x1 += v.y;
           }
-          const bool ok0 = !bad && (all_in || row_valid<MODE>(sref, s * kT + tp, L));
-          const bool ok1 = !bad && (all_in || row_valid<MODE>(sref, s * kT + tp + 1, L));
+          const bool ok0 = !bad & (all_in | row_valid<MODE>(sref, s * kT + tp, L));
+          const bool ok1 = !bad & (all_in | row_valid<MODE>(sref, s * kT + tp + 1, L));
           x0 = ok0 ? x0 * p.scale_log2 : -INFINITY;
           x1 = ok1 ? x1 * p.scale_log2 : -INFINITY;
           float tmax = fmaxf(x0, x1);
           tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
           tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
           tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
-          float alpha = 1.f;
-          if (tmax > m_run + 8.f) {  // lazy rescale: keep a stale max while P <= 2^8
-            alpha = ex2(m_run - tmax);  // m_run = -inf gives 0
-            m_run = tmax;
-          }
+          // lazy rescale: keep a stale max while P <= 2^8 (m_run = -inf gives alpha = 0)
+          const bool upd = tmax > m_run + 8.f;
+          const float alpha = upd ? ex2(m_run - tmax) : 1.f;
+          m_run = upd ? tmax : m_run;
           const float mref = (m_run == -INFINITY) ? 0.f : m_run;  // nothing valid yet: x = -inf -> p = 0
           const float p0 = ex2(x0 - mref), p1 = ex2(x1 - mref);
           l_run = l_run * alpha + (p0 + p1);
+#if MLAQ_TC_AGG
+          {
+            // P^T[head hh][k] with token k order matching the TMEM A columns
+            const int kp = tp < 8 ? 2 * tp : 2 * tp - 14;
+            const int off = (hh >> 3) * 256 + (kp >> 3) * 128 + (hh & 7) * 16 + (kp & 7) * 2;
+            *reinterpret_cast<__half2*>(&sm.pt[ab][off]) = __floats2half2_rn(p0, p1);
+            fence_view_async_shared();
+            const bool any_rs = __any_sync(0xffffffffu, alpha != 1.f);
+            if (lane == 0) sm.rescale_flag[w] = any_rs;
+          }
+#else
           *reinterpret_cast<__half2*>(&sm.pr[hh][tp]) = __floats2half2_rn(p0, p1);
+#endif
           if ((lane & 7) == 0) sm.alpha[hh] = alpha;
         }
         named_bar_sync(2, kThreads);
+        // ---------------- aggregation
+#if MLAQ_TC_AGG
+        {
+          const bool need_rs = !item_first && (sm.rescale_flag[0] | sm.rescale_flag[1] | sm.rescale_flag[2] |
+                                               sm.rescale_flag[3]);
+          if (need_rs) {  // rare (lazy max): scale O^T columns by alpha[head]
+            const int lp = agg_ctr - 1;
+            mbar_wait_bounded(&sm.agg_done[lp % kAggBufs], (lp / kAggBufs) & 1, kWaitLimit);
+            tc_fence_after();
+            float al[16];
+#pragma unroll
+            for (int h = 0; h < 16; ++h) al[h] = sm.alpha[h];
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) {
+              uint32_t v[16];
+              const uint32_t ta = tmem + ((uint32_t)(32 * w) << 16) + (uint32_t)(16 * blk);
+              tmem_ld_32x32b_x16(ta, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int h = 0; h < 16; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * al[h]);
+              tmem_st_32x32b_x16(ta, v);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            named_bar_sync(3, kThreads);
+            tc_fence_after();
+          }
+          if (lane == 0) {
+            tc_fence_after();
+            const uint64_t bdesc = umma_smem_desc(smem_u32(sm.pt[ab]), 128, 256);
+            umma_f16_ts(tmem + (uint32_t)(16 * w), tmem + (uint32_t)(kTmemA + 32 * ab + 8 * w), bdesc, kAggIdesc,
+                        !item_first);
+            umma_commit(&sm.agg_done[ab]);
+          }
+          __syncwarp();
+          item_first = false;
+          agg_ctr++;
+        }
+#else
         // ---------------- aggregation
         {
           const float ar = sm.alpha[r], ar8 = sm.alpha[r + 8];
@@ -714,6 +824,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
               mma16816(o[j][kk][1], pa, ch[j][kk][2], ch[j][kk][3]);
             }
         }
+#endif
         // No barrier before the next step's writes to sp: every thread passed
         // barrier 2 after all reads of sp; pr/alpha are rewritten only after
         // the next barrier 1, which all threads reach after their reads.
@@ -731,6 +842,33 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
     }
     __syncthreads();
     float* op = p.o_part + ((size_t)item_idx * H + h0) * kDL;
+#if MLAQ_TC_AGG
+    {
+      // O^T lane l of block blk holds channel 128 (l/32) + 64 (blk/2) + 16 (2 (blk%2) + (l%32)/16) + l%16
+      if (agg_ctr > 0) {
+        const int lp = agg_ctr - 1;
+        mbar_wait_bounded(&sm.agg_done[lp % kAggBufs], (lp / kAggBufs) & 1, kWaitLimit);
+      }
+      tc_fence_after();
+      float inv[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        const float l = sm.fin_l[h];
+        inv[h] = l > 0.f ? 1.f / l : 0.f;
+      }
+      const int x = lane;
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk) {
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(tmem + ((uint32_t)(32 * w) << 16) + (uint32_t)(16 * blk), v);
+        tmem_wait_ld();
+        const int c = 128 * w + 64 * (blk >> 1) + 16 * (2 * (blk & 1) + (x >> 4)) + (x & 15);
+#pragma unroll
+        for (int h = 0; h < 16; ++h) op[(size_t)h * kDL + c] = inv[h] != 0.f ? __uint_as_float(v[h]) * inv[h] : 0.f;
+      }
+      tc_fence_before();
+    }
+#else
     {
       const float lr0 = sm.fin_l[r], lr8 = sm.fin_l[r + 8];
       const float inv0 = lr0 > 0.f ? 1.f / lr0 : 0.f, inv8 = lr8 > 0.f ? 1.f / lr8 : 0.f;
@@ -747,6 +885,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
                 make_float2(o[j][kk][cb][2] * inv8, o[j][kk][cb][3] * inv8);
           }
     }
+#endif
     if (tid < 16) {
       const float l = sm.fin_l[tid];
       p.lse_part[(size_t)item_idx * H + h0 + tid] =
@@ -811,6 +950,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
     for (int gg = g_fail; gg < pc.issued; ++gg)
       mbar_wait_bounded(&sm.full[gg % kStages], (gg / kStages) & 1, kWaitLimit);
   }
+#if MLAQ_TC_AGG
+  // every aggregation MMA has completed (waited for in each item epilogue)
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (w == 0) tmem_dealloc(tmem, kTmemCols);
+#endif
 }
 
 // ---------------------------------------------------------------------------
@@ -950,7 +1096,7 @@ int launch_decode_static(int mode, const void* codes, const void* meta, const vo
   c.workspace = g_static_ptr[dev];
   c.workspace_bytes = kStaticScratchBytes;
   c.num_sms = g_static_sms[dev];
-  c.decode_ctas = 2 * c.num_sms < kMaxPlanCtas ? 2 * c.num_sms : kMaxPlanCtas;
+  c.decode_ctas = MLAQ_CTAS_PER_SM * c.num_sms < kMaxPlanCtas ? MLAQ_CTAS_PER_SM * c.num_sms : kMaxPlanCtas;
   char* ws = static_cast<char*>(c.workspace);
   // the status word is sticky: start each call from zero
   if (cudaMemsetAsync(ws + kWsStatus, 0, sizeof(int), s) != cudaSuccess) return MLAQ_ERR_CUDA;
