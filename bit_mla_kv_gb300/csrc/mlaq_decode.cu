@@ -207,8 +207,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, in
   __syncthreads();
   for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + tid;
-    int cnt = 0, c_lo = 0, c_hi = -1, u0 = 0, u1 = 0;
+    int cnt = 0, c_lo = 0, c_hi = -1, u0 = 0, u1 = 0, Lb = 0;
     if (b < B) {
+      Lb = clamp_len(p.seq_lens[b], p.max_tokens);
       u0 = useq[b];
       u1 = useq[b + 1];
       if (u1 > u0) {
@@ -224,7 +225,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, in
       int k = carry + ex;
       item_start[b] = k;
       for (int c = c_lo; c <= c_hi; ++c)
-        if (bnd[c] < bnd[c + 1]) items[k++] = Item{b, max(bnd[c], u0) - u0, min(bnd[c + 1], u1) - u0, c};
+        if (bnd[c] < bnd[c + 1])
+          items[k++] = Item{b, max(bnd[c], u0) - u0, min(bnd[c + 1], u1) - u0, c, Lb, 0, 0, 0};
     }
     __syncthreads();
     if (tid == 0) carry_s = carry + tot;
@@ -333,7 +335,7 @@ __device__ __forceinline__ bool row_valid(const StageRef& st, int j, int L) {
 
 // Producer: issue the bulk copies of a stage into buffer `buf`.
 template <int MODE>
-__device__ void issue_stage(const DecodeParams& p, DecodeSmem& sm, int b, const StageRef& st, int buf) {
+__device__ void issue_stage(const DecodeParams& p, DecodeSmem& sm, int b, const StageRef& st, int page, int buf) {
   uint64_t* bar = &sm.full[buf];
   if (st.kind == 0) {
     const int base = kT * st.idx;
@@ -344,9 +346,6 @@ __device__ void issue_stage(const DecodeParams& p, DecodeSmem& sm, int b, const 
     bulk_g2s(sm.stage[buf], p.ring + ((size_t)b * kRing + base) * kD, bytes, bar);
     return;
   }
-  const int pidx = st.kind == 1 ? st.idx : st.idx / 4;
-  int page = -1;
-  if (pidx < p.max_pages) page = p.page_table[(size_t)b * p.max_pages + pidx];
   if (page < 0 || page >= p.num_pages) {
     atomicOr(p.status, MLAQ_DEV_PAGE_OOB);
     sm.stage_bad[buf] = 1;
@@ -367,27 +366,48 @@ __device__ void issue_stage(const DecodeParams& p, DecodeSmem& sm, int b, const 
   }
 }
 
-// Producer cursor over the CTA's stage stream (all its items, in order).
+// Page-table entry of stage k of item `it` (-1 when out of the table); ring
+// chunks need none.
+template <int MODE>
+__device__ __forceinline__ int stage_page(const DecodeParams& p, const Item& it, int k) {
+  const StageRef st = item_stage<MODE>(it, it.L, k);
+  if (st.kind == 0) return 0;
+  const int pidx = st.kind == 1 ? st.idx : st.idx / 4;
+  return pidx < p.max_pages ? p.page_table[(size_t)it.b * p.max_pages + pidx] : -1;
+}
+
+// Producer cursor over the CTA's stage stream (all its items, in order). The
+// page-table entry of the stage at the cursor and the item after the current
+// one are loaded one call ahead, so issuing a stage never waits on a global
+// load.
 struct ProdCursor {
-  int item, k, nst, b, L, issued;
+  int item, k, nst, issued, page;
+  Item cur, nxt;
 };
 template <int MODE>
+__device__ void producer_init(const DecodeParams& p, ProdCursor& pc, int i0, int i1) {
+  pc.item = i0;
+  pc.k = 0;
+  pc.issued = 0;
+  pc.cur = p.items[i0];
+  pc.nst = item_stages<MODE>(pc.cur, pc.cur.L);
+  if (i0 + 1 < i1) pc.nxt = p.items[i0 + 1];
+  pc.page = stage_page<MODE>(p, pc.cur, 0);
+}
+template <int MODE>
 __device__ void producer_advance(const DecodeParams& p, DecodeSmem& sm, ProdCursor& pc, int i1) {
-  while (pc.item < i1 && pc.k >= pc.nst) {  // step to the next item with stages
+  if (pc.item >= i1) return;
+  issue_stage<MODE>(p, sm, pc.cur.b, item_stage<MODE>(pc.cur, pc.cur.L, pc.k), pc.page, pc.issued % kStages);
+  pc.issued++;
+  if (++pc.k >= pc.nst) {  // items always have at least one stage
     pc.item++;
     pc.k = 0;
-    if (pc.item < i1) {
-      const Item it = p.items[pc.item];
-      pc.b = it.b;
-      pc.L = clamp_len(p.seq_lens[it.b], p.max_tokens);
-      pc.nst = item_stages<MODE>(it, pc.L);
-    }
+    if (pc.item >= i1) return;
+    pc.cur = pc.nxt;
+    pc.nst = item_stages<MODE>(pc.cur, pc.cur.L);
+    if (pc.item + 1 < i1) pc.nxt = p.items[pc.item + 1];
   }
-  if (pc.item >= i1) return;
-  const Item it = p.items[pc.item];
-  issue_stage<MODE>(p, sm, pc.b, item_stage<MODE>(it, pc.L, pc.k), pc.issued % kStages);
-  pc.k++;
-  pc.issued++;
+  pc.page = stage_page<MODE>(p, pc.cur, pc.k);
 }
 
 template <int MODE>
@@ -431,13 +451,7 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
 #endif
   ProdCursor pc;
   if (tid == 0) {
-    const Item it = p.items[i0];
-    pc.item = i0;
-    pc.k = 0;
-    pc.b = it.b;
-    pc.L = clamp_len(p.seq_lens[it.b], p.max_tokens);
-    pc.nst = item_stages<MODE>(it, pc.L);
-    pc.issued = 0;
+    producer_init<MODE>(p, pc, i0, i1);
     for (int s = 0; s < kStages; ++s) producer_advance<MODE>(p, sm, pc, i1);
   }
 
@@ -451,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
 
   for (int item_idx = i0; item_idx < i1; ++item_idx) {
     const Item it = p.items[item_idx];
-    const int L = clamp_len(p.seq_lens[it.b], p.max_tokens);
+    const int L = it.L;
     if (it.b != cur_b) {
       cur_b = it.b;
       // query fragments (B operand of the score MMA: k = channel, n = head)
@@ -731,14 +745,19 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
           const bool ok1 = !bad & (all_in | row_valid<MODE>(sref, s * kT + tp + 1, L));
           x0 = ok0 ? x0 * p.scale_log2 : -INFINITY;
           x1 = ok1 ? x1 * p.scale_log2 : -INFINITY;
-          float tmax = fmaxf(x0, x1);
-          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
-          // lazy rescale: keep a stale max while P <= 2^8 (m_run = -inf gives alpha = 0)
-          const bool upd = tmax > m_run + 8.f;
-          const float alpha = upd ? ex2(m_run - tmax) : 1.f;
-          m_run = upd ? tmax : m_run;
+          // Lazy rescale: keep a stale running max while every P <= 2^8. The
+          // tile max (three shuffles) is only needed when some score exceeds
+          // it by more than 8 (log2 units), e.g. on an item's first tile.
+          float alpha = 1.f;
+          if (__any_sync(0xffffffffu, fmaxf(x0, x1) > m_run + 8.f)) {
+            float tmax = fmaxf(x0, x1);
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+            const bool upd = tmax > m_run + 8.f;  // m_run = -inf gives alpha = 0
+            alpha = upd ? ex2(m_run - tmax) : 1.f;
+            m_run = upd ? tmax : m_run;
+          }
           const float mref = (m_run == -INFINITY) ? 0.f : m_run;  // nothing valid yet: x = -inf -> p = 0
           const float p0 = ex2(x0 - mref), p1 = ex2(x1 - mref);
           l_run = l_run * alpha + (p0 + p1);

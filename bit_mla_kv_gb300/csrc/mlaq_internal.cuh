@@ -49,8 +49,9 @@ __host__ __device__ constexpr int page_code_bytes(int mode) { return kPage * tok
 // processed by CTA `cta`. A sequence's units are its ring chunks (16 BF16
 // sink/recent slots each; packed modes) followed by its packed pages (4 units
 // = 4 steps of 16 tokens each) or, in BF16 mode, 16-token quarter pages.
-struct Item {
+struct __align__(16) Item {
   int b, u_lo, u_hi, cta;
+  int L, pad0, pad1, pad2;  // L: the sequence's (clamped) length when the plan was made
 };
 
 // Items: at most one per sequence plus one per CTA boundary inside a sequence.
