@@ -69,8 +69,9 @@ struct DecodeParams {
   const Item* items;
   const int* item_start;
   const int* cta_item_start;
+  const Item* cta_first;  // first item of each CTA; pad0 = page of its first stage
   int* counters;
-  float* o_part;
+  __half* o_part;  // normalized split partials, fp16
   float* lse_part;
   uint16_t* out;
   float* lse;
@@ -142,16 +143,40 @@ __device__ __forceinline__ int last_le(const int* a, int lo, int hi, int key) {
   return lo;
 }
 
-// Planner: one CTA of 1024 threads, on the device (no host sync).
-__global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, int G, int* useq, int* bnd, int* ne,
-                                                    Item* items, int* item_start, int* cta_item_start,
-                                                    int* num_items) {
+// Planner: one CTA of 1024 threads, on the device (no host sync). Its working
+// arrays live in dynamic shared memory, so no pass waits on dependent
+// global-memory loads: useq[B+1] (unit prefix), sitem[B+1] (first item of
+// each sequence), bnd[G+1] (CTA boundaries), ne[G+1] (non-empty CTAs below).
+__host__ __device__ inline size_t plan_smem_bytes(int B, int G) {
+  return (size_t)(2 * (B + 1) + 2 * (G + 1)) * sizeof(int);
+}
+// Page-table entry of an item's first stage (0 for a ring chunk, -1 when the
+// page index is outside the table).
+__device__ __forceinline__ int first_stage_page(const DecodeParams& p, int mode, const Item& it) {
+  int pidx;
+  if (mode == MLAQ_BF16) {
+    pidx = it.u_lo / 4;
+  } else {
+    const int R = ring_units(mode, it.L);
+    if (it.u_lo < R) return 0;
+    pidx = (it.u_lo - R) / 4;
+  }
+  return pidx < p.max_pages ? p.page_table[(size_t)it.b * p.max_pages + pidx] : -1;
+}
+
+__global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, int G, Item* items, int* item_start,
+                                                    int* cta_item_start, Item* cta_first, int* num_items) {
+  extern __shared__ int plan_smem[];
   __shared__ int red[32];
   __shared__ int carry_s;
   const int tid = threadIdx.x;
   const int B = p.B;
-  // A: units per sequence, exclusive prefix in useq; reset combine counters;
-  //    empty sequences get out = 0, lse = -inf here.
+  int* useq = plan_smem;
+  int* sitem = useq + (B + 1);
+  int* bnd = sitem + (B + 1);
+  int* ne = bnd + (G + 1);
+  // A: units per sequence -> useq (exclusive prefix); reset the merge
+  //    counters; empty sequences get out = 0, lse = -inf.
   if (tid == 0) carry_s = 0;
   __syncthreads();
   for (int base = 0; base < B; base += blockDim.x) {
@@ -193,7 +218,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, in
     bnd[c] = v;
   }
   __syncthreads();
-  // C: ne[c] = number of non-empty CTAs below c
+  // C: ne[c] = number of non-empty CTAs below c (G + 1 <= 1024)
   {
     const int c = tid;
     const int nonempty = (c < G && bnd[c] < bnd[c + 1]) ? 1 : 0;
@@ -224,6 +249,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, in
     if (b < B) {
       int k = carry + ex;
       item_start[b] = k;
+      sitem[b] = k;
       for (int c = c_lo; c <= c_hi; ++c)
         if (bnd[c] < bnd[c + 1])
           items[k++] = Item{b, max(bnd[c], u0) - u0, min(bnd[c + 1], u1) - u0, c, Lb, 0, 0, 0};
@@ -237,15 +263,25 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, in
     item_start[B] = n;
     *num_items = n;
   }
-  __syncthreads();
-  // E: first item of every CTA (items are ordered by CTA)
+  // E: first item of every CTA. Items are ordered by unit position; the first
+  // item at or after unit bnd[c] (in sequence bs) is the first item of bs plus
+  // the non-empty CTAs between the first CTA of bs and c. An empty CTA gets
+  // the same value as the next non-empty one, so its item range is empty.
   for (int c = tid; c <= G; c += blockDim.x) {
-    int lo = 0, hi = n;  // first j with items[j].cta >= c
-    while (lo < hi) {
-      int mid = (lo + hi) >> 1;
-      if (items[mid].cta < c) lo = mid + 1; else hi = mid;
+    int v = n;
+    if (bnd[c] < U) {
+      const int bs = last_le(useq, 0, B, bnd[c]);
+      const int c_lo = last_le(bnd, 0, G - 1, useq[bs]);
+      v = sitem[bs] + ne[c] - ne[c_lo];
     }
-    cta_item_start[c] = lo;
+    cta_item_start[c] = v;
+    // the CTA's first item, with the page of its first stage, so that the
+    // decode CTA can issue its first copy after a single load
+    if (c < G && v < n) {
+      Item f = items[v];
+      f.pad0 = first_stage_page(p, mode, f);
+      cta_first[c] = f;
+    }
   }
 }
 
@@ -356,8 +392,7 @@ __device__ void issue_stage(const DecodeParams& p, DecodeSmem& sm, int b, const 
   if constexpr (MODE == MLAQ_BF16) {
     const uint32_t bytes = kT * kD * 2;
     mbar_arrive_expect_tx(bar, bytes);
-    bulk_g2s(sm.stage[buf], p.codes + (size_t)page * page_code_bytes(MODE) + (size_t)(st.idx % 4) * bytes, bytes,
-             bar);
+    bulk_g2s(sm.stage[buf], p.codes + (size_t)page * page_code_bytes(MODE) + (size_t)(st.idx % 4) * bytes, bytes, bar);
   } else {
     const uint32_t cb = page_code_bytes(MODE);
     mbar_arrive_expect_tx(bar, cb + kMetaPage);
@@ -385,14 +420,14 @@ struct ProdCursor {
   Item cur, nxt;
 };
 template <int MODE>
-__device__ void producer_init(const DecodeParams& p, ProdCursor& pc, int i0, int i1) {
+__device__ void producer_init(const DecodeParams& p, ProdCursor& pc, const Item& first, int i0, int i1) {
   pc.item = i0;
   pc.k = 0;
   pc.issued = 0;
-  pc.cur = p.items[i0];
+  pc.cur = first;  // the planner's copy of items[i0], pad0 = page of stage 0
   pc.nst = item_stages<MODE>(pc.cur, pc.cur.L);
   if (i0 + 1 < i1) pc.nxt = p.items[i0 + 1];
-  pc.page = stage_page<MODE>(p, pc.cur, 0);
+  pc.page = first.pad0;
 }
 template <int MODE>
 __device__ void producer_advance(const DecodeParams& p, DecodeSmem& sm, ProdCursor& pc, int i1) {
@@ -415,6 +450,8 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
   extern __shared__ __align__(128) uint8_t smem_raw[];
   DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
   const int cta = blockIdx.y;
+  // issued together: the CTA's item range and its first item
+  const Item first = threadIdx.x == 0 ? p.cta_first[cta] : Item{};
   const int i0 = p.cta_item_start[cta], i1 = p.cta_item_start[cta + 1];
   if (i0 >= i1) return;
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
@@ -451,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
 #endif
   ProdCursor pc;
   if (tid == 0) {
-    producer_init<MODE>(p, pc, i0, i1);
+    producer_init<MODE>(p, pc, first, i0, i1);
     for (int s = 0; s < kStages; ++s) producer_advance<MODE>(p, sm, pc, i1);
   }
 
@@ -860,7 +897,7 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
       sm.fin_l[hh] = failed ? 0.f : l_tot;
     }
     __syncthreads();
-    float* op = p.o_part + ((size_t)item_idx * H + h0) * kDL;
+    __half* op = p.o_part + ((size_t)item_idx * H + h0) * kDL;
 #if MLAQ_TC_AGG
     {
       // O^T lane l of block blk holds channel 128 (l/32) + 64 (blk/2) + 16 (2 (blk%2) + (l%32)/16) + l%16
@@ -883,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
         tmem_wait_ld();
         const int c = 128 * w + 64 * (blk >> 1) + 16 * (2 * (blk & 1) + (x >> 4)) + (x & 15);
 #pragma unroll
-        for (int h = 0; h < 16; ++h) op[(size_t)h * kDL + c] = inv[h] != 0.f ? __uint_as_float(v[h]) * inv[h] : 0.f;
+        for (int h = 0; h < 16; ++h) op[(size_t)h * kDL + c] = __float2half_rn(inv[h] != 0.f ? __uint_as_float(v[h]) * inv[h] : 0.f);
       }
       tc_fence_before();
     }
@@ -898,10 +935,10 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
 #pragma unroll
           for (int cb = 0; cb < 2; ++cb) {
             const int c = 64 * (2 * w + j) + 16 * kk + 8 * cb + 2 * i;
-            *reinterpret_cast<float2*>(op + (size_t)r * kDL + c) =
-                make_float2(o[j][kk][cb][0] * inv0, o[j][kk][cb][1] * inv0);
-            *reinterpret_cast<float2*>(op + (size_t)(r + 8) * kDL + c) =
-                make_float2(o[j][kk][cb][2] * inv8, o[j][kk][cb][3] * inv8);
+            *reinterpret_cast<__half2*>(op + (size_t)r * kDL + c) =
+                __floats2half2_rn(o[j][kk][cb][0] * inv0, o[j][kk][cb][1] * inv0);
+            *reinterpret_cast<__half2*>(op + (size_t)(r + 8) * kDL + c) =
+                __floats2half2_rn(o[j][kk][cb][2] * inv8, o[j][kk][cb][3] * inv8);
           }
     }
 #endif
@@ -924,25 +961,59 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
       const int s0 = p.item_start[it.b], s1 = p.item_start[it.b + 1];
       const int hc = tid >> 3, cc = (tid & 7) * 64;  // head h0+hc, channels cc..cc+63
       const int row = h0 + hc;
+      // max over the partial lse values (loads issued four at a time)
       float m = -INFINITY;
-      for (int sidx = s0; sidx < s1; ++sidx) m = fmaxf(m, __ldcg(&p.lse_part[(size_t)sidx * H + row]));
+      int sidx = s0;
+      for (; sidx + 4 <= s1; sidx += 4) {
+        const float l0 = __ldcg(&p.lse_part[(size_t)(sidx + 0) * H + row]);
+        const float l1 = __ldcg(&p.lse_part[(size_t)(sidx + 1) * H + row]);
+        const float l2 = __ldcg(&p.lse_part[(size_t)(sidx + 2) * H + row]);
+        const float l3 = __ldcg(&p.lse_part[(size_t)(sidx + 3) * H + row]);
+        m = fmaxf(m, fmaxf(fmaxf(l0, l1), fmaxf(l2, l3)));
+      }
+      for (; sidx < s1; ++sidx) m = fmaxf(m, __ldcg(&p.lse_part[(size_t)sidx * H + row]));
       float acc[64];
 #pragma unroll
       for (int e = 0; e < 64; ++e) acc[e] = 0.f;
       float tot = 0.f;
       if (m != -INFINITY) {
-        for (int sidx = s0; sidx < s1; ++sidx) {
+        // four partials per iteration: 32 independent 16-byte loads in flight
+        auto accum = [&](const uint4& u, float wgt, int q) {
+          const __half2* hv = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(hv[e]);
+            acc[8 * q + 2 * e] = fmaf(wgt, f.x, acc[8 * q + 2 * e]);
+            acc[8 * q + 2 * e + 1] = fmaf(wgt, f.y, acc[8 * q + 2 * e + 1]);
+          }
+        };
+        for (sidx = s0; sidx + 4 <= s1; sidx += 4) {
+          float wv[4];
+          uint4 v[4][8];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            wv[u] = __ldcg(&p.lse_part[(size_t)(sidx + u) * H + row]);
+            const uint4* src = reinterpret_cast<const uint4*>(p.o_part + ((size_t)(sidx + u) * H + row) * kDL + cc);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[u][q] = __ldcg(src + q);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float wgt = expf(wv[u] - m);
+            tot += wgt;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) accum(v[u][q], wgt, q);
+          }
+        }
+        for (; sidx < s1; ++sidx) {
           const float wgt = expf(__ldcg(&p.lse_part[(size_t)sidx * H + row]) - m);
           tot += wgt;
-          const float4* src = reinterpret_cast<const float4*>(p.o_part + ((size_t)sidx * H + row) * kDL + cc);
+          const uint4* src = reinterpret_cast<const uint4*>(p.o_part + ((size_t)sidx * H + row) * kDL + cc);
+          uint4 v[8];
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const float4 v = __ldcg(src + q);
-            acc[4 * q + 0] = fmaf(wgt, v.x, acc[4 * q + 0]);
-            acc[4 * q + 1] = fmaf(wgt, v.y, acc[4 * q + 1]);
-            acc[4 * q + 2] = fmaf(wgt, v.z, acc[4 * q + 2]);
-            acc[4 * q + 3] = fmaf(wgt, v.w, acc[4 * q + 3]);
-          }
+          for (int q = 0; q < 8; ++q) v[q] = __ldcg(src + q);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) accum(v[q], wgt, q);
         }
       }
       const float inv = tot > 0.f ? 1.f / tot : 0.f;
@@ -1029,8 +1100,9 @@ cudaError_t launch_decode(mlaq_cache* c, const uint16_t* q_latent, const uint16_
   p.items = reinterpret_cast<const Item*>(ws + lay.items);
   p.item_start = reinterpret_cast<const int*>(ws + lay.item_start);
   p.cta_item_start = reinterpret_cast<const int*>(ws + lay.cta_item_start);
+  p.cta_first = reinterpret_cast<const Item*>(ws + lay.cta_first);
   p.counters = reinterpret_cast<int*>(ws + lay.counters);
-  p.o_part = reinterpret_cast<float*>(ws + lay.o_part);
+  p.o_part = reinterpret_cast<__half*>(ws + lay.o_part);
   p.lse_part = reinterpret_cast<float*>(ws + lay.lse_part);
   p.out = out;
   p.lse = lse;
@@ -1042,11 +1114,24 @@ cudaError_t launch_decode(mlaq_cache* c, const uint16_t* q_latent, const uint16_
   p.max_tokens = c->max_pages_per_seq * kPage;
   p.scale_log2 = scale * 1.4426950408889634f;
 
-  plan_kernel<<<1, 1024, 0, s>>>(p, c->mode, G, reinterpret_cast<int*>(ws + lay.useq),
-                                 reinterpret_cast<int*>(ws + lay.bnd), reinterpret_cast<int*>(ws + lay.nonempty),
-                                 reinterpret_cast<Item*>(ws + lay.items), reinterpret_cast<int*>(ws + lay.item_start),
-                                 reinterpret_cast<int*>(ws + lay.cta_item_start),
-                                 reinterpret_cast<int*>(ws + kWsNumItems));
+  {
+    // the planner's shared-memory arrays exceed 48 KB for large batches
+    static bool plan_attr_done[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t ea = cudaGetDevice(&dev);
+    if (ea != cudaSuccess) return ea;
+    if (dev < 0 || dev >= kMaxDevices || !plan_attr_done[dev]) {
+      ea = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)plan_smem_bytes(kMaxSeqs, kMaxPlanCtas));
+      if (ea != cudaSuccess) return ea;
+      if (dev >= 0 && dev < kMaxDevices) plan_attr_done[dev] = true;
+    }
+  }
+  plan_kernel<<<1, 1024, plan_smem_bytes(B, G), s>>>(p, c->mode, G, reinterpret_cast<Item*>(ws + lay.items),
+                                                     reinterpret_cast<int*>(ws + lay.item_start),
+                                                     reinterpret_cast<int*>(ws + lay.cta_item_start),
+                                                     reinterpret_cast<Item*>(ws + lay.cta_first),
+                                                     reinterpret_cast<int*>(ws + kWsNumItems));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (c->mode == MLAQ_C4R4) return run_decode<MLAQ_C4R4>(c, p, G, s);

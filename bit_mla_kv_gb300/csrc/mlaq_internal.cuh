@@ -62,7 +62,7 @@ inline size_t max_partial_rows(int max_seqs, int max_heads) {
 }
 
 struct WsLayout {
-  size_t items, item_start, useq, bnd, nonempty, cta_item_start, counters, lse_part, o_part, total;
+  size_t items, item_start, cta_first, cta_item_start, counters, lse_part, o_part, total;
 };
 inline WsLayout ws_layout(int max_seqs, int max_heads) {
   auto al = [](size_t x) { return (x + 255) / 256 * 256; };
@@ -70,14 +70,12 @@ inline WsLayout ws_layout(int max_seqs, int max_heads) {
   size_t off = 256;
   L.items = off;          off += al(max_items_for(max_seqs) * sizeof(Item));
   L.item_start = off;     off += al(((size_t)max_seqs + 1) * 4);
-  L.useq = off;           off += al(((size_t)max_seqs + 1) * 4);
-  L.bnd = off;            off += al(((size_t)kMaxPlanCtas + 1) * 4);
-  L.nonempty = off;       off += al(((size_t)kMaxPlanCtas + 2) * 4);
+  L.cta_first = off;      off += al(((size_t)kMaxPlanCtas + 1) * sizeof(Item));
   L.cta_item_start = off; off += al(((size_t)kMaxPlanCtas + 1) * 4);
   L.counters = off;       off += al((size_t)max_seqs * kMaxHeadBlocks * 4);
   const size_t rows = max_partial_rows(max_seqs, max_heads);
   L.lse_part = off;       off += al(rows * 4);
-  L.o_part = off;         off += rows * kDL * 4;
+  L.o_part = off;         off += rows * kDL * 2;  // fp16 partial outputs
   L.total = off;
   return L;
 }
