@@ -655,23 +655,27 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
             mx[j] = v0 ? one : 0u;
             my[j] = v1 ? one : 0u;
           }
-          const uint8_t* rx = st + lr * (kD * 2);
-          const uint8_t* ry = st + (lr + 8) * (kD * 2);
+          // rows lr and lr + 8 share lr mod 8 = r, so both use the chunk
+          // permutation of r; channels c and c + 8 are adjacent chunks
+          const uint16_t* rx = reinterpret_cast<const uint16_t*>(st + lr * (kD * 2));
+          const uint16_t* ry = reinterpret_cast<const uint16_t*>(st + (lr + 8) * (kD * 2));
 #pragma unroll
           for (int j = 0; j < 2; ++j)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const int c = 64 * (2 * w + j) + 16 * kk + 2 * i;
-              ch[j][kk][0] = v0 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(rx + 2 * c)) : 0u;
-              ch[j][kk][1] = v1 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(ry + 2 * c)) : 0u;
-              ch[j][kk][2] = v0 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(rx + 2 * c + 16)) : 0u;
-              ch[j][kk][3] = v1 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(ry + 2 * c + 16)) : 0u;
+              const int e0 = bf16_row_pos(c, r), e1 = bf16_row_pos(c + 8, r);
+              ch[j][kk][0] = v0 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(rx + e0)) : 0u;
+              ch[j][kk][1] = v1 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(ry + e0)) : 0u;
+              ch[j][kk][2] = v0 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(rx + e1)) : 0u;
+              ch[j][kk][3] = v1 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(ry + e1)) : 0u;
             }
           const int c = kDL + 16 * w + 2 * i;
-          rf[0] = v0 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(rx + 2 * c)) : 0u;
-          rf[1] = v1 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(ry + 2 * c)) : 0u;
-          rf[2] = v0 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(rx + 2 * c + 16)) : 0u;
-          rf[3] = v1 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(ry + 2 * c + 16)) : 0u;
+          const int e0 = bf16_row_pos(c, r), e1 = bf16_row_pos(c + 8, r);
+          rf[0] = v0 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(rx + e0)) : 0u;
+          rf[1] = v1 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(ry + e0)) : 0u;
+          rf[2] = v0 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(rx + e1)) : 0u;
+          rf[3] = v1 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(ry + e1)) : 0u;
         }
         // min term: S += [mn_j (hi, lo) rows] . [K2_j hi, lo]
         {

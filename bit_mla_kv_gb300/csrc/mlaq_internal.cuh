@@ -80,6 +80,10 @@ inline WsLayout ws_layout(int max_seqs, int max_heads) {
   return L;
 }
 
+// BF16 rows (ring slots, BF16-mode page tokens): element position of channel
+// e in row r; the 16-byte chunks are XOR-permuted by r mod 8.
+__host__ __device__ inline int bf16_row_pos(int e, int r) { return (((e >> 3) ^ (r & 7)) << 3) | (e & 7); }
+
 // ---------------------------------------------------------------------------
 // Physical code layout inside a token's bytes.
 //

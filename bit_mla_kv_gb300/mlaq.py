@@ -99,6 +99,16 @@ def buffer_sizes(mode: str, num_pages: int, max_seqs: int, max_heads: int):
     return tuple(o.value for o in out)
 
 
+def _bf16_rows_in_channel_order(raw):
+    """Undo the stored chunk permutation of BF16 rows: channel e of row r
+    sits at element ((e // 8) ^ (r % 8)) * 8 + e % 8 of the row."""
+    rows = raw.shape[-2]
+    e = torch.arange(576)
+    r = torch.arange(rows)[:, None]
+    idx = (((e // 8) ^ (r % 8)) * 8 + e % 8).to(raw.device)
+    return torch.gather(raw, -1, idx.expand(raw.shape))
+
+
 class Cache:
     """A paged QuantMLA cache: the code pool, fp16 meta pool, BF16 sink/recent
     ring and workspace are torch device tensors owned by this object."""
@@ -131,9 +141,18 @@ class Cache:
         return self._h
 
     def ring_view(self):
-        """The BF16 ring as [max_seqs, 132, 576] bfloat16 (slots 0-3 sink,
-        slot 4 + t % 128 for recent token t)."""
-        return self.ring[: self.max_seqs * 132 * 576 * 2].view(torch.bfloat16).view(self.max_seqs, 132, 576)
+        """The BF16 ring as [max_seqs, 132, 576] bfloat16 in channel order
+        (slots 0-3 sink, slot 4 + t % 128 for recent token t); a copy, with
+        the stored chunk permutation undone."""
+        raw = self.ring[: self.max_seqs * 132 * 576 * 2].view(torch.bfloat16).view(self.max_seqs, 132, 576)
+        return _bf16_rows_in_channel_order(raw)
+
+    def bf16_pages_view(self):
+        """BF16 mode: the page pool as [num_pages, 64, 576] bfloat16 in
+        channel order (a copy)."""
+        assert self.mode == "BF16"
+        raw = self.codes[: self.num_pages * 64 * 576 * 2].view(torch.bfloat16).view(self.num_pages, 64, 576)
+        return _bf16_rows_in_channel_order(raw)
 
     def append(self, page_table, seq_lens, c_latent, k_rope, cu_new=None, stream=None):
         """Append tokens. Without cu_new: c_latent [B, n_new, 512], k_rope

@@ -88,6 +88,11 @@ typedef enum mlaq_status {
  *              (0 for BF16);
  *   ring:      BF16 sink + recent buffer, 132 tokens x 1152 B per sequence
  *              slot (0 for BF16);
+ * BF16 rows (ring slots, and tokens of BF16-mode pages) keep their 72
+ * 16-byte chunks XOR-permuted by the row index: channel e of row r (r = ring
+ * slot, or token index within its page) is element
+ * ((e / 8) ^ (r % 8)) * 8 + e % 8 of the row, so that eight consecutive rows
+ * read at one channel fall in eight different shared-memory bank groups.
  *   workspace: split-KV plan, partial outputs and the device status word,
  *              for batches up to max_seqs sequences and max_heads heads.
  * Limits: 1 <= max_seqs <= 16384; max_heads a multiple of 16 in [16, 128].

@@ -92,3 +92,20 @@ def test_code_layout_is_a_bijection():
         assert cells == list(range(64))
         assert all(content_bit(c, bits) % bits == 0 for c in range(64))
     assert sorted(rope_bit(c) // 4 for c in range(64)) == list(range(64))
+
+
+def test_bf16_row_chunk_permutation():
+    # The binding's inverse of the stored BF16 row order (header: channel e of
+    # row r at ((e / 8) ^ (r % 8)) * 8 + e % 8) undoes a forward scatter, and
+    # the 8 rows of one fragment read one channel from 8 distinct chunks mod 8.
+    import torch
+    from bit_mla_kv_gb300.mlaq import _bf16_rows_in_channel_order
+    rows = 132
+    logical = torch.arange(rows * 576, dtype=torch.float32).view(1, rows, 576)
+    stored = torch.empty_like(logical)
+    for r in range(rows):
+        for e in range(576):
+            stored[0, r, ((e // 8) ^ (r % 8)) * 8 + e % 8] = logical[0, r, e]
+    assert torch.equal(_bf16_rows_in_channel_order(stored), logical)
+    for e in range(0, 576, 8):
+        assert sorted((((e // 8) ^ r) * 8) // 8 % 8 for r in range(8)) == list(range(8))

@@ -51,7 +51,7 @@ def test_writer_codes_meta_ring_bit_exact(mode):
 def test_writer_bf16_pages_hold_tokens():
     case = Case("BF16", [1, 64, 65, 300], 16, seed=12)
     case.build()
-    pages = case.cache.codes.view(torch.bfloat16).view(-1, 64, 576).cpu()
+    pages = case.cache.bf16_pages_view().cpu()
     for b, L in enumerate(case.seq_lens):
         tok = torch.from_numpy(case.tokens(b))
         for t in range(L):
