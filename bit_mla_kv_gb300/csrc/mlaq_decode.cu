@@ -105,6 +105,19 @@ __device__ __forceinline__ int seq_units(int mode, int L) {
   const int pages = L > kRing ? (L - kRecent + kPage - 1) / kPage : 0;
   return ring_units(mode, L) + 4 * pages;
 }
+// Planning cost, in quarter steps: a packed or BF16-page step (16 tokens)
+// costs 4, a ring step 5 (its BF16 tile takes about 1.3x the time of a
+// packed one on GB300). cost_to_unit maps a cost offset inside a sequence,
+// snapped to a step boundary, back to its unit index.
+constexpr int kCostStep = 4, kCostRing = 5;
+__device__ __forceinline__ int seq_cost(int mode, int L) {
+  const int R = ring_units(mode, L);
+  return kCostRing * R + kCostStep * (seq_units(mode, L) - R);
+}
+__device__ __forceinline__ int cost_to_unit(int mode, int L, int x) {
+  const int R = ring_units(mode, L);
+  return x < kCostRing * R ? x / kCostRing : R + (x - kCostRing * R) / kCostStep;
+}
 
 // ---------------------------------------------------------------------------
 // Block-wide exclusive scan of one int per thread (blockDim.x == 1024).
@@ -186,7 +199,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, in
       const int Lraw = p.seq_lens[b];
       if (Lraw > p.max_tokens) atomicOr(p.status, MLAQ_DEV_SEQ_OVERFLOW);
       const int L = clamp_len(Lraw, p.max_tokens);
-      u = seq_units(mode, L);
+      u = seq_cost(mode, L);
       for (int hb = 0; hb < p.HB; ++hb) p.counters[b * kMaxHeadBlocks + hb] = 0;
       if (L == 0) {
         for (int k = 0; k < p.H * kDL; ++k) p.out[(size_t)b * p.H * kDL + k] = 0;
@@ -204,15 +217,21 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, in
   if (tid == 0) useq[B] = carry_s;
   __syncthreads();
   const int U = useq[B];
-  // B: CTA boundaries, snapped down to a page start inside packed pages.
+  // B: CTA boundaries (in cost), snapped down to a step start, and to a page
+  //    start inside packed pages.
   for (int c = tid; c <= G; c += blockDim.x) {
     const int raw = (int)(((long long)c * U) / G);
     int v = raw;
     if (raw < U) {
       const int b = last_le(useq, 0, B, raw);
       const int R = ring_units(mode, clamp_len(p.seq_lens[b], p.max_tokens));
+      const int xr = kCostRing * R;
       int x = raw - useq[b];
-      if (mode != MLAQ_BF16 && x > R) x = R + ((x - R) / 4) * 4;
+      if (x < xr)
+        x = (x / kCostRing) * kCostRing;
+      else
+        x = xr + ((x - xr) / (mode == MLAQ_BF16 ? kCostStep : 4 * kCostStep)) *
+                     (mode == MLAQ_BF16 ? kCostStep : 4 * kCostStep);
       v = useq[b] + x;
     }
     bnd[c] = v;
@@ -252,7 +271,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, in
       sitem[b] = k;
       for (int c = c_lo; c <= c_hi; ++c)
         if (bnd[c] < bnd[c + 1])
-          items[k++] = Item{b, max(bnd[c], u0) - u0, min(bnd[c + 1], u1) - u0, c, Lb, 0, 0, 0};
+          items[k++] = Item{b, cost_to_unit(mode, Lb, max(bnd[c], u0) - u0),
+                            cost_to_unit(mode, Lb, min(bnd[c + 1], u1) - u0), c, Lb, 0, 0, 0};
     }
     __syncthreads();
     if (tid == 0) carry_s = carry + tot;
