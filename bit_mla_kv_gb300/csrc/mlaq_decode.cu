@@ -49,6 +49,10 @@ constexpr int kSpStride = 20;                         // floats per row of parti
 constexpr int kPStride = 24;                          // halfs per row of P [h][t]
 constexpr uint64_t kWaitLimit = 200000000ull;  // 200 ms per bounded wait
 constexpr int kMaxDevices = 64;
+template <bool B>
+struct BoolC {
+  static constexpr bool value = B;
+};
 #ifndef MLAQ_TC_AGG
 #define MLAQ_TC_AGG 0
 #endif
@@ -597,16 +601,21 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
       const StageRef sref = item_stage<MODE>(it, L, k);
       const bool packed = sref.kind == 1;
       const int nsteps = packed ? kPage / kT : 1;
-      for (int s = 0; s < nsteps; ++s) {
+      // One 16-token step. FULL: a packed step of a live stage whose 16 rows
+      // are all valid (inside [4, L - 128)), the common case, compiled
+      // without any per-row masking.
+      auto step_body = [&](auto full_c, const int s) -> bool {
+        constexpr bool FULL = decltype(full_c)::value;
+        const bool packed_s = FULL || packed;
         const int lr = s * kT + r;  // row of token r in the stage
-        bool all_in = false;        // every row of the step valid (common inside a packed range)
-        if (packed) {
+        bool all_in = FULL;         // every row of the step valid
+        if (!FULL && packed) {
           const int t0 = kPage * sref.idx + s * kT;
           all_in = t0 >= kSink && t0 + kT <= L - kRecent;
         }
-        const bool live = ok & !bad;
-        const bool v0 = live & (all_in | row_valid<MODE>(sref, lr, L));
-        const bool v1 = live & (all_in | row_valid<MODE>(sref, lr + 8, L));
+        const bool live = FULL || (ok & !bad);
+        const bool v0 = FULL || (live & (all_in | row_valid<MODE>(sref, lr, L)));
+        const bool v1 = FULL || (live & (all_in | row_valid<MODE>(sref, lr + 8, L)));
         // ---------------- dequant + scores
         uint32_t mx[3], my[3];  // meta (s, mn) of tokens r (x) and r+8 (y), groups 2w, 2w+1, rope
         uint32_t ch[2][4][4];   // fp16 A fragments of the content tile (exact codes, later dequantized)
@@ -616,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
         for (int hb = 0; hb < 2; ++hb)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sacc[hb][e] = 0.f;
-        if (packed) {
+        if (packed_s) {
           const uint8_t* mtab = st + page_code_bytes(MODE);
 #pragma unroll
           for (int j = 0; j < 3; ++j) {
@@ -785,11 +794,7 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
         const bool agg_ok = true;
 #endif
         // barrier 1: partial scores complete; also agrees on a timed-out wait
-        if (named_bar_or(1, kThreads, !(ok && agg_ok))) {
-          failed = true;
-          g_fail = g - 1;
-          break;
-        }
+        if (named_bar_or(1, kThreads, !(ok && agg_ok))) return true;
         // the stage's shared memory is no longer read: refill it with the
         // next stage of the CTA's stream
         if (tid == 0 && s == nsteps - 1) producer_advance<MODE>(p, sm, pc, i1);
@@ -802,8 +807,8 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
             x0 += v.x;
             x1 += v.y;
           }
-          const bool ok0 = !bad & (all_in | row_valid<MODE>(sref, s * kT + tp, L));
-          const bool ok1 = !bad & (all_in | row_valid<MODE>(sref, s * kT + tp + 1, L));
+          const bool ok0 = FULL || (!bad & (all_in | row_valid<MODE>(sref, s * kT + tp, L)));
+          const bool ok1 = FULL || (!bad & (all_in | row_valid<MODE>(sref, s * kT + tp + 1, L)));
           x0 = ok0 ? x0 * p.scale_log2 : -INFINITY;
           x1 = ok1 ? x1 * p.scale_log2 : -INFINITY;
           // Lazy rescale: keep a stale running max while every P <= 2^8. The
@@ -908,6 +913,26 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
         // No barrier before the next step's writes to sp: every thread passed
         // barrier 2 after all reads of sp; pr/alpha are rewritten only after
         // the next barrier 1, which all threads reach after their reads.
+        return false;
+      };
+      for (int s = 0; s < nsteps; ++s) {
+        bool full = false;
+        if (packed) {
+          const int t0 = kPage * sref.idx + s * kT;
+          full = ok & !bad & (t0 >= kSink) & (t0 + kT <= L - kRecent);
+        }
+        // both variants meet at the same named barriers, so threads that
+        // disagree on `full` (a timed-out wait is per thread) stay in step
+        bool fail;
+        if constexpr (MODE == MLAQ_BF16)
+          fail = step_body(BoolC<false>{}, s);  // no packed steps
+        else
+          fail = full ? step_body(BoolC<true>{}, s) : step_body(BoolC<false>{}, s);
+        if (fail) {
+          failed = true;
+          g_fail = g - 1;
+          break;
+        }
       }
     }
 
@@ -985,17 +1010,22 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
       const int s0 = p.item_start[it.b], s1 = p.item_start[it.b + 1];
       const int hc = tid >> 3, cc = (tid & 7) * 64;  // head h0+hc, channels cc..cc+63
       const int row = h0 + hc;
-      // max over the partial lse values (loads issued four at a time)
+      // partial lse values of all items of the sequence: one parallel load
+      // into shared memory (the partial-score buffer is free here), then
+      // each thread takes the max for its head
+      float* lse_s = &sm.sp[0][0][0];
+      constexpr int kLseCap = (int)(sizeof(sm.sp) / sizeof(float)) / 16;  // items per pass
+      const int n_part = s1 - s0;
       float m = -INFINITY;
-      int sidx = s0;
-      for (; sidx + 4 <= s1; sidx += 4) {
-        const float l0 = __ldcg(&p.lse_part[(size_t)(sidx + 0) * H + row]);
-        const float l1 = __ldcg(&p.lse_part[(size_t)(sidx + 1) * H + row]);
-        const float l2 = __ldcg(&p.lse_part[(size_t)(sidx + 2) * H + row]);
-        const float l3 = __ldcg(&p.lse_part[(size_t)(sidx + 3) * H + row]);
-        m = fmaxf(m, fmaxf(fmaxf(l0, l1), fmaxf(l2, l3)));
+      for (int base = 0; base < n_part; base += kLseCap) {
+        const int cnt = min(kLseCap, n_part - base);
+        for (int k = tid; k < cnt * 16; k += kThreads)
+          lse_s[k] = __ldcg(&p.lse_part[(size_t)(s0 + base + (k >> 4)) * H + h0 + (k & 15)]);
+        __syncthreads();
+        for (int k = 0; k < cnt; ++k) m = fmaxf(m, lse_s[k * 16 + hc]);
+        __syncthreads();
       }
-      for (; sidx < s1; ++sidx) m = fmaxf(m, __ldcg(&p.lse_part[(size_t)sidx * H + row]));
+      int sidx = s0;
       float acc[64];
 #pragma unroll
       for (int e = 0; e < 64; ++e) acc[e] = 0.f;
