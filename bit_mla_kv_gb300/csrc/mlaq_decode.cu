@@ -45,8 +45,8 @@ constexpr int kStages = MLAQ_STAGES;
 constexpr int kT = 16;                                // tokens per step
 constexpr int kRingChunks = (kRing + kT - 1) / kT;    // 9
 constexpr int kStageBytes = kPage * 288 + kMetaPage;  // 20736: max(C4R4 page + meta, 16 BF16 tokens)
-constexpr int kSpStride = 20;                         // floats per row of partial scores [h][t]
-constexpr int kPStride = 24;                          // halfs per row of P [h][t]
+constexpr int kSpStride = 52;  // floats per row of partial scores [h][t] (32 tokens; 52 = 20 mod 32)
+constexpr int kPStride = 40;   // halfs per row of P [h][t] (32 tokens; 80-byte rows for ldmatrix)
 constexpr uint64_t kWaitLimit = 200000000ull;  // 200 ms per bounded wait
 constexpr int kMaxDevices = 64;
 template <bool B>
@@ -915,6 +915,229 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
         // the next barrier 1, which all threads reach after their reads.
         return false;
       };
+#if !MLAQ_TC_AGG
+      // Half a packed page (32 tokens, all valid) as two 16-token sub-steps
+      // under one pair of barriers: half the synchronisation per token of
+      // the 16-token step. The dequantized, transposed content fragments of
+      // both sub-steps stay in registers until the aggregation.
+      auto half_body = [&](const int s2) -> bool {
+        uint32_t vt[2][2][4][4];
+        const uint8_t* mtab = st + page_code_bytes(MODE);
+#pragma unroll
+        for (int sub = 0; sub < 2; ++sub) {
+          const int lr = 32 * s2 + 16 * sub + r;
+          uint32_t mx[3], my[3];
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            const int gg = j < 2 ? 2 * w + j : 8;
+            mx[j] = *reinterpret_cast<const uint32_t*>(mtab + lr * kMetaTok + 4 * gg);
+            my[j] = *reinterpret_cast<const uint32_t*>(mtab + (lr + 8) * kMetaTok + 4 * gg);
+          }
+          uint32_t (&ch)[2][4][4] = vt[sub];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int gg = 2 * w + j;
+            if constexpr (CBITS == 4) {
+              const uint2 wx = *reinterpret_cast<const uint2*>(st + lr * CB + gg * GBYTES + 8 * i);
+              const uint2 wy = *reinterpret_cast<const uint2*>(st + (lr + 8) * CB + gg * GBYTES + 8 * i);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t ax = (kk >> 1) ? wx.y : wx.x, ay = (kk >> 1) ? wy.y : wy.x;
+                const uint32_t ax8 = ax >> 8, ay8 = ay >> 8;
+                const int p0 = 2 * (kk & 1);
+                ch[j][kk][0] = int4_pos(ax, ax8, p0);
+                ch[j][kk][1] = int4_pos(ay, ay8, p0);
+                ch[j][kk][2] = int4_pos(ax, ax8, p0 + 1);
+                ch[j][kk][3] = int4_pos(ay, ay8, p0 + 1);
+              }
+            } else {
+              const uint32_t ax = *reinterpret_cast<const uint32_t*>(st + lr * CB + gg * GBYTES + 4 * i);
+              const uint32_t ay = *reinterpret_cast<const uint32_t*>(st + (lr + 8) * CB + gg * GBYTES + 4 * i);
+              const uint32_t ax8 = ax >> 8, ay8 = ay >> 8;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                ch[j][kk][0] = int2_pos(ax, ax8, 2 * kk);
+                ch[j][kk][1] = int2_pos(ay, ay8, 2 * kk);
+                ch[j][kk][2] = int2_pos(ax, ax8, 2 * kk + 1);
+                ch[j][kk][3] = int2_pos(ay, ay8, 2 * kk + 1);
+              }
+            }
+          }
+          uint32_t rf[4];
+          {
+            uint32_t ax = *reinterpret_cast<const uint32_t*>(st + lr * CB + ROPE_OFF + 4 * (2 * w + (i >> 1)));
+            uint32_t ay = *reinterpret_cast<const uint32_t*>(st + (lr + 8) * CB + ROPE_OFF + 4 * (2 * w + (i >> 1)));
+            if (i & 1) {
+              ax >>= 8;
+              ay >>= 8;
+            }
+            rf[0] = int4_pos(ax, 0u, 0);
+            rf[1] = int4_pos(ay, 0u, 0);
+            rf[2] = int4_pos(ax, 0u, 1);
+            rf[3] = int4_pos(ay, 0u, 1);
+          }
+          float sacc[2][4];
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[hb][e] = 0.f;
+          {
+            uint32_t a[4];
+            const uint32_t mnx = (i == 0) ? mx[0] : (i == 1) ? mx[1] : mx[2];
+            const uint32_t mny = (i == 0) ? my[0] : (i == 1) ? my[1] : my[2];
+            a[0] = (i < 3) ? __byte_perm(mnx, 0, 0x3232) : 0u;
+            a[1] = (i < 3) ? __byte_perm(mny, 0, 0x3232) : 0u;
+            a[2] = 0u;
+            a[3] = 0u;
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) mma16816(sacc[hb], a, kmn[hb], 0u);
+          }
+          {
+            float d0[2][4], d1[2][4], d2[2][4];
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) d0[hb][e] = d1[hb][e] = d2[hb][e] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              mma16816(d0[0], ch[0][kk], qf[0][kk][0][0], qf[0][kk][0][1]);
+              mma16816(d1[0], ch[1][kk], qf[1][kk][0][0], qf[1][kk][0][1]);
+              mma16816(d0[1], ch[0][kk], qf[0][kk][1][0], qf[0][kk][1][1]);
+              mma16816(d1[1], ch[1][kk], qf[1][kk][1][0], qf[1][kk][1][1]);
+            }
+            mma16816(d2[0], rf, qr[0][0], qr[0][1]);
+            mma16816(d2[1], rf, qr[1][0], qr[1][1]);
+            float sxv[3], syv[3];
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+              sxv[j] = __half2float(__ushort_as_half((unsigned short)(mx[j] & 0xffffu)));
+              syv[j] = __half2float(__ushort_as_half((unsigned short)(my[j] & 0xffffu)));
+            }
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+              sacc[hb][0] = fmaf(sxv[2], d2[hb][0], fmaf(sxv[1], d1[hb][0], fmaf(sxv[0], d0[hb][0], sacc[hb][0])));
+              sacc[hb][1] = fmaf(sxv[2], d2[hb][1], fmaf(sxv[1], d1[hb][1], fmaf(sxv[0], d0[hb][1], sacc[hb][1])));
+              sacc[hb][2] = fmaf(syv[2], d2[hb][2], fmaf(syv[1], d1[hb][2], fmaf(syv[0], d0[hb][2], sacc[hb][2])));
+              sacc[hb][3] = fmaf(syv[2], d2[hb][3], fmaf(syv[1], d1[hb][3], fmaf(syv[0], d0[hb][3], sacc[hb][3])));
+            }
+          }
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            const int h = 8 * hb + 2 * i;
+            const int t = 16 * sub + r;
+            sm.sp[w][h][t] = sacc[hb][0];
+            sm.sp[w][h + 1][t] = sacc[hb][1];
+            sm.sp[w][h][t + 8] = sacc[hb][2];
+            sm.sp[w][h + 1][t + 8] = sacc[hb][3];
+          }
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const __half2 s2x = __low2half2(u32_as_h2(mx[j])), m2x = __high2half2(u32_as_h2(mx[j]));
+            const __half2 s2y = __low2half2(u32_as_h2(my[j])), m2y = __high2half2(u32_as_h2(my[j]));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              ch[j][kk][0] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][0]), s2x, m2x)));
+              ch[j][kk][1] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][1]), s2y, m2y)));
+              ch[j][kk][2] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][2]), s2x, m2x)));
+              ch[j][kk][3] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][3]), s2y, m2y)));
+            }
+          }
+        }
+        // barrier 1: partial scores of 32 tokens complete; agrees on a timed-out wait
+        if (named_bar_or(1, kThreads, !ok)) return true;
+        if (tid == 0 && s2 == 1) producer_advance<MODE>(p, sm, pc, i1);
+        // online softmax for head hh, tokens tq .. tq + 3
+        {
+          const int tq = 4 * (lane & 7);
+          float x[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int ww = 0; ww < kWarps; ++ww) {
+            const float4 v = *reinterpret_cast<const float4*>(&sm.sp[ww][hh][tq]);
+            x[0] += v.x;
+            x[1] += v.y;
+            x[2] += v.z;
+            x[3] += v.w;
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) x[u] *= p.scale_log2;
+          const float xm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+          float alpha = 1.f;
+          if (__any_sync(0xffffffffu, xm > m_run + 8.f)) {
+            float tmax = xm;
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+            const bool upd = tmax > m_run + 8.f;
+            alpha = upd ? ex2(m_run - tmax) : 1.f;
+            m_run = upd ? tmax : m_run;
+          }
+          const float p0 = ex2(x[0] - m_run), p1 = ex2(x[1] - m_run);
+          const float p2 = ex2(x[2] - m_run), p3 = ex2(x[3] - m_run);
+          l_run = l_run * alpha + ((p0 + p1) + (p2 + p3));
+          const __half2 q01 = __floats2half2_rn(p0, p1), q23 = __floats2half2_rn(p2, p3);
+          *reinterpret_cast<uint2*>(&sm.pr[hh][tq]) = make_uint2(h2_as_u32(q01), h2_as_u32(q23));
+          if ((lane & 7) == 0) sm.alpha[hh] = alpha;
+        }
+        named_bar_sync(2, kThreads);
+        // aggregation over both sub-steps
+        {
+          const float ar = sm.alpha[r], ar8 = sm.alpha[r + 8];
+          if (__any_sync(0xffffffffu, ar != 1.f || ar8 != 1.f)) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                for (int cb = 0; cb < 2; ++cb) {
+                  o[j][kk][cb][0] *= ar;
+                  o[j][kk][cb][1] *= ar;
+                  o[j][kk][cb][2] *= ar8;
+                  o[j][kk][cb][3] *= ar8;
+                }
+          }
+          uint32_t pa[2][4];
+          ldmatrix_x4(pa[0], &sm.pr[(lane & 7) + 8 * ((lane >> 3) & 1)][8 * (lane >> 4)]);
+          ldmatrix_x4(pa[1], &sm.pr[(lane & 7) + 8 * ((lane >> 3) & 1)][16 + 8 * (lane >> 4)]);
+#pragma unroll
+          for (int sub = 0; sub < 2; ++sub)
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                mma16816(o[j][kk][0], pa[sub], vt[sub][j][kk][0], vt[sub][j][kk][1]);
+                mma16816(o[j][kk][1], pa[sub], vt[sub][j][kk][2], vt[sub][j][kk][3]);
+              }
+        }
+        return false;
+      };
+#endif
+#if !MLAQ_TC_AGG
+      if constexpr (MODE != MLAQ_BF16) {
+        // packed stage: all-valid halves take the 32-token body; the decision
+        // uses only CTA-uniform values (a timed-out wait is caught at barrier 1)
+        if (packed) {
+          bool fail = false;
+          for (int s2 = 0; s2 < 2 && !fail; ++s2) {
+            const int t0 = kPage * sref.idx + 32 * s2;
+            if (!bad && t0 >= kSink && t0 + 32 <= L - kRecent) {
+              fail = half_body(s2);
+            } else {
+              for (int q = 0; q < 2 && !fail; ++q) {
+                const int s = 2 * s2 + q;
+                const int t1 = t0 + kT * q;
+                const bool full = ok & !bad & (t1 >= kSink) & (t1 + kT <= L - kRecent);
+                fail = full ? step_body(BoolC<true>{}, s) : step_body(BoolC<false>{}, s);
+              }
+            }
+          }
+          if (fail) {
+            failed = true;
+            g_fail = g - 1;
+          }
+          continue;
+        }
+      }
+#endif
       for (int s = 0; s < nsteps; ++s) {
         bool full = false;
         if (packed) {
