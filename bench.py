@@ -300,7 +300,7 @@ def run_mlaq(args, ws, rank, local):
         roof = {"bound": "tensor", "achieved": achieved, "peak": tf_burst, "unit": "TFLOP/s",
                 "frac": achieved / tf_burst, "peak_source": f"{peak_src} bf16_tflops (burst)"}
     roof["traffic"] = recorded_traffic(args.workload)
-    roof["kernel"] = "mlaq::decode_kernel (split-KV attention)"
+    roof["kernel"] = "mlaq_decode: plan_kernel + decode_kernel (split-KV attention) + combine_kernel"
     roof["kernel_ms"] = kern_avg
     roof["roofline_us"] = max(t_mem, t_ten) * 1e6
     roof["frac_of_roofline_kernel"] = max(t_mem, t_ten) * 1e3 / kern_avg

@@ -56,10 +56,12 @@ struct BoolC {
 #ifndef MLAQ_TC_AGG
 #define MLAQ_TC_AGG 0
 #endif
+#if MLAQ_TC_AGG
 // Aggregation on tcgen05 (MLAQ_TC_AGG): O^T[channel][head] accumulates in TMEM.
 constexpr int kAggBufs = 2;      // A (content) / P^T step buffers in flight
 constexpr int kTmemCols = 128;   // O^T: 4 blocks x 16 heads; A: 2 buffers x 4 blocks x 8 columns
 constexpr int kTmemA = 64;       // first column of the A step buffers
+#endif
 
 struct DecodeParams {
   const uint8_t* codes;
@@ -74,7 +76,6 @@ struct DecodeParams {
   const int* item_start;
   const int* cta_item_start;
   const Item* cta_first;  // first item of each CTA; pad0 = page of its first stage
-  int* counters;
   __half* o_part;  // normalized split partials, fp16
   float* lse_part;
   uint16_t* out;
@@ -91,7 +92,6 @@ struct __align__(16) DecodeSmem {
   float fin_m[16];
   float fin_l[16];
   int stage_bad[kStages];
-  int is_last;
   uint64_t full[kStages];
 #if MLAQ_TC_AGG
   __align__(128) uint8_t pt[kAggBufs][512];  // P^T B operand: 16 heads x 16 tokens, 8x8 core matrices
@@ -186,6 +186,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, in
   extern __shared__ int plan_smem[];
   __shared__ int red[32];
   __shared__ int carry_s;
+  pdl_wait();               // seq_lens may come from the kernel before
+  pdl_launch_dependents();  // the decode grid may launch and wait for this one
   const int tid = threadIdx.x;
   const int B = p.B;
   int* useq = plan_smem;
@@ -193,7 +195,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, in
   int* bnd = sitem + (B + 1);
   int* ne = bnd + (G + 1);
   // A: units per sequence -> useq (exclusive prefix); reset the merge
-  //    counters; empty sequences get out = 0, lse = -inf.
+  //    empty sequences get out = 0, lse = -inf.
   if (tid == 0) carry_s = 0;
   __syncthreads();
   for (int base = 0; base < B; base += blockDim.x) {
@@ -204,7 +206,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, in
       if (Lraw > p.max_tokens) atomicOr(p.status, MLAQ_DEV_SEQ_OVERFLOW);
       const int L = clamp_len(Lraw, p.max_tokens);
       u = seq_cost(mode, L);
-      for (int hb = 0; hb < p.HB; ++hb) p.counters[b * kMaxHeadBlocks + hb] = 0;
       if (L == 0) {
         for (int k = 0; k < p.H * kDL; ++k) p.out[(size_t)b * p.H * kDL + k] = 0;
         for (int h = 0; h < p.H; ++h) p.lse[(size_t)b * p.H + h] = -INFINITY;
@@ -474,6 +475,8 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
   extern __shared__ __align__(128) uint8_t smem_raw[];
   DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
   const int cta = blockIdx.y;
+  pdl_wait();  // the plan
+  pdl_launch_dependents();
   // issued together: the CTA's item range and its first item
   const Item first = threadIdx.x == 0 ? p.cta_first[cta] : Item{};
   const int i0 = p.cta_item_start[cta], i1 = p.cta_item_start[cta + 1];
@@ -527,6 +530,7 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
   for (int item_idx = i0; item_idx < i1; ++item_idx) {
     const Item it = p.items[item_idx];
     const int L = it.L;
+    const bool single = p.item_start[it.b + 1] - p.item_start[it.b] == 1;
     if (it.b != cur_b) {
       cur_b = it.b;
       // query fragments (B operand of the score MMA: k = channel, n = head)
@@ -1169,6 +1173,8 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
       sm.fin_l[hh] = failed ? 0.f : l_tot;
     }
     __syncthreads();
+    // A sequence with a single item is final here (bf16 out, lse); otherwise
+    // the normalized partial (fp16) and its lse go to the combine kernel.
     __half* op = p.o_part + ((size_t)item_idx * H + h0) * kDL;
 #if MLAQ_TC_AGG
     {
@@ -1192,7 +1198,13 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
         tmem_wait_ld();
         const int c = 128 * w + 64 * (blk >> 1) + 16 * (2 * (blk & 1) + (x >> 4)) + (x & 15);
 #pragma unroll
-        for (int h = 0; h < 16; ++h) op[(size_t)h * kDL + c] = __float2half_rn(inv[h] != 0.f ? __uint_as_float(v[h]) * inv[h] : 0.f);
+        for (int h = 0; h < 16; ++h) {
+          const float val = inv[h] != 0.f ? __uint_as_float(v[h]) * inv[h] : 0.f;
+          if (single)
+            p.out[((size_t)it.b * H + h0 + h) * kDL + c] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+          else
+            op[(size_t)h * kDL + c] = __float2half_rn(val);
+        }
       }
       tc_fence_before();
     }
@@ -1200,6 +1212,7 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
     {
       const float lr0 = sm.fin_l[r], lr8 = sm.fin_l[r + 8];
       const float inv0 = lr0 > 0.f ? 1.f / lr0 : 0.f, inv8 = lr8 > 0.f ? 1.f / lr8 : 0.f;
+      uint16_t* fo = p.out + ((size_t)it.b * H + h0) * kDL;
 #pragma unroll
       for (int j = 0; j < 2; ++j)
 #pragma unroll
@@ -1207,108 +1220,29 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
 #pragma unroll
           for (int cb = 0; cb < 2; ++cb) {
             const int c = 64 * (2 * w + j) + 16 * kk + 8 * cb + 2 * i;
-            *reinterpret_cast<__half2*>(op + (size_t)r * kDL + c) =
-                __floats2half2_rn(o[j][kk][cb][0] * inv0, o[j][kk][cb][1] * inv0);
-            *reinterpret_cast<__half2*>(op + (size_t)(r + 8) * kDL + c) =
-                __floats2half2_rn(o[j][kk][cb][2] * inv8, o[j][kk][cb][3] * inv8);
+            if (single) {
+              const __nv_bfloat162 v0 = __floats2bfloat162_rn(o[j][kk][cb][0] * inv0, o[j][kk][cb][1] * inv0);
+              const __nv_bfloat162 v1 = __floats2bfloat162_rn(o[j][kk][cb][2] * inv8, o[j][kk][cb][3] * inv8);
+              *reinterpret_cast<__nv_bfloat162*>(fo + (size_t)r * kDL + c) = v0;
+              *reinterpret_cast<__nv_bfloat162*>(fo + (size_t)(r + 8) * kDL + c) = v1;
+            } else {
+              *reinterpret_cast<__half2*>(op + (size_t)r * kDL + c) =
+                  __floats2half2_rn(o[j][kk][cb][0] * inv0, o[j][kk][cb][1] * inv0);
+              *reinterpret_cast<__half2*>(op + (size_t)(r + 8) * kDL + c) =
+                  __floats2half2_rn(o[j][kk][cb][2] * inv8, o[j][kk][cb][3] * inv8);
+            }
           }
     }
 #endif
     if (tid < 16) {
       const float l = sm.fin_l[tid];
-      p.lse_part[(size_t)item_idx * H + h0 + tid] =
-          l > 0.f ? (sm.fin_m[tid] + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      const float lse_v = l > 0.f ? (sm.fin_m[tid] + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      if (single)
+        p.lse[(size_t)it.b * H + h0 + tid] = lse_v;
+      else
+        p.lse_part[(size_t)item_idx * H + h0 + tid] = lse_v;
     }
-    // ---- the last CTA to finish a sequence merges its partials
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-      const int n_items = p.item_start[it.b + 1] - p.item_start[it.b];
-      const int old = atomicAdd(&p.counters[it.b * kMaxHeadBlocks + hb_idx], 1);
-      sm.is_last = (old == n_items - 1);
-    }
-    __syncthreads();
-    if (sm.is_last) {
-      __threadfence();
-      const int s0 = p.item_start[it.b], s1 = p.item_start[it.b + 1];
-      const int hc = tid >> 3, cc = (tid & 7) * 64;  // head h0+hc, channels cc..cc+63
-      const int row = h0 + hc;
-      // partial lse values of all items of the sequence: one parallel load
-      // into shared memory (the partial-score buffer is free here), then
-      // each thread takes the max for its head
-      float* lse_s = &sm.sp[0][0][0];
-      constexpr int kLseCap = (int)(sizeof(sm.sp) / sizeof(float)) / 16;  // items per pass
-      const int n_part = s1 - s0;
-      float m = -INFINITY;
-      for (int base = 0; base < n_part; base += kLseCap) {
-        const int cnt = min(kLseCap, n_part - base);
-        for (int k = tid; k < cnt * 16; k += kThreads)
-          lse_s[k] = __ldcg(&p.lse_part[(size_t)(s0 + base + (k >> 4)) * H + h0 + (k & 15)]);
-        __syncthreads();
-        for (int k = 0; k < cnt; ++k) m = fmaxf(m, lse_s[k * 16 + hc]);
-        __syncthreads();
-      }
-      int sidx = s0;
-      float acc[64];
-#pragma unroll
-      for (int e = 0; e < 64; ++e) acc[e] = 0.f;
-      float tot = 0.f;
-      if (m != -INFINITY) {
-        // four partials per iteration: 32 independent 16-byte loads in flight
-        auto accum = [&](const uint4& u, float wgt, int q) {
-          const __half2* hv = reinterpret_cast<const __half2*>(&u);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __half22float2(hv[e]);
-            acc[8 * q + 2 * e] = fmaf(wgt, f.x, acc[8 * q + 2 * e]);
-            acc[8 * q + 2 * e + 1] = fmaf(wgt, f.y, acc[8 * q + 2 * e + 1]);
-          }
-        };
-        for (sidx = s0; sidx + 4 <= s1; sidx += 4) {
-          float wv[4];
-          uint4 v[4][8];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            wv[u] = __ldcg(&p.lse_part[(size_t)(sidx + u) * H + row]);
-            const uint4* src = reinterpret_cast<const uint4*>(p.o_part + ((size_t)(sidx + u) * H + row) * kDL + cc);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) v[u][q] = __ldcg(src + q);
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float wgt = expf(wv[u] - m);
-            tot += wgt;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) accum(v[u][q], wgt, q);
-          }
-        }
-        for (; sidx < s1; ++sidx) {
-          const float wgt = expf(__ldcg(&p.lse_part[(size_t)sidx * H + row]) - m);
-          tot += wgt;
-          const uint4* src = reinterpret_cast<const uint4*>(p.o_part + ((size_t)sidx * H + row) * kDL + cc);
-          uint4 v[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) v[q] = __ldcg(src + q);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) accum(v[q], wgt, q);
-        }
-      }
-      const float inv = tot > 0.f ? 1.f / tot : 0.f;
-      uint16_t* dst = p.out + ((size_t)it.b * H + row) * kDL + cc;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        uint4 pk;
-        uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          __nv_bfloat162 v = __floats2bfloat162_rn(acc[8 * q + 2 * e] * inv, acc[8 * q + 2 * e + 1] * inv);
-          pw[e] = *reinterpret_cast<uint32_t*>(&v);
-        }
-        *reinterpret_cast<uint4*>(dst + 8 * q) = pk;
-      }
-      if ((tid & 7) == 0) p.lse[(size_t)it.b * H + row] = tot > 0.f ? m + logf(tot) : -INFINITY;
-    }
-    __syncthreads();  // sm.is_last / fin_* are reused by the next item
+    __syncthreads();  // fin_* are reused by the next item
   }
 
   if (failed && tid == 0) {
@@ -1327,6 +1261,93 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
 }
 
 // ---------------------------------------------------------------------------
+// ---------------------------------------------------------------------------
+// Combine (split-KV): for every sequence with more than one item, the
+// normalized partials O_k and their lse_k merge into
+//   out = sum_k exp(lse_k - M) O_k / sum_k exp(lse_k - M),  lse = M + log(sum_k exp(lse_k - M)).
+// One work unit = (sequence, head block, 64-channel chunk); a thread owns one
+// head and 8 channels, so all partials of a unit are read in one batch.
+constexpr int kCombineBatch = 16;
+__global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
+  pdl_wait();
+  const int tid = threadIdx.x;
+  const int hc = tid >> 3, c8 = (tid & 7) * 8;
+  const int units = p.B * p.HB * 8;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int chunk = u & 7, rest = u >> 3;
+    const int hb = rest % p.HB, b = rest / p.HB;
+    const int s0 = p.item_start[b], s1 = p.item_start[b + 1];
+    if (s1 - s0 < 2) continue;  // finalized by the decode kernel
+    const int row = 16 * hb + hc;
+    const int c = 64 * chunk + c8;
+    float m = -INFINITY;
+    for (int k0 = s0; k0 < s1; k0 += kCombineBatch) {
+      float l[kCombineBatch];
+#pragma unroll
+      for (int k = 0; k < kCombineBatch; ++k)
+        l[k] = k0 + k < s1 ? __ldcg(&p.lse_part[(size_t)(k0 + k) * p.H + row]) : -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kCombineBatch; ++k) m = fmaxf(m, l[k]);
+    }
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float tot = 0.f;
+    if (m != -INFINITY) {
+      for (int k0 = s0; k0 < s1; k0 += kCombineBatch) {
+        uint4 v[kCombineBatch];
+        float l[kCombineBatch];
+#pragma unroll
+        for (int k = 0; k < kCombineBatch; ++k) {
+          const bool in = k0 + k < s1;
+          l[k] = in ? __ldcg(&p.lse_part[(size_t)(k0 + k) * p.H + row]) : -INFINITY;
+          v[k] = in ? __ldcg(reinterpret_cast<const uint4*>(p.o_part + ((size_t)(k0 + k) * p.H + row) * kDL + c))
+                    : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < kCombineBatch; ++k) {
+          const float wgt = expf(l[k] - m);  // 0 for padding (lse = -inf)
+          tot += wgt;
+          const __half2* hv = reinterpret_cast<const __half2*>(&v[k]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(hv[e]);
+            acc[2 * e] = fmaf(wgt, f.x, acc[2 * e]);
+            acc[2 * e + 1] = fmaf(wgt, f.y, acc[2 * e + 1]);
+          }
+        }
+      }
+    }
+    const float inv = tot > 0.f ? 1.f / tot : 0.f;
+    uint4 pk;
+    uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 bv = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+      pw[e] = *reinterpret_cast<const uint32_t*>(&bv);
+    }
+    *reinterpret_cast<uint4*>(p.out + ((size_t)b * p.H + row) * kDL + c) = pk;
+    if (chunk == 0 && (tid & 7) == 0) p.lse[(size_t)b * p.H + row] = tot > 0.f ? m + logf(tot) : -INFINITY;
+  }
+}
+
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel in the stream finishes; it calls pdl_wait() before it
+// reads anything that kernel wrote.
+template <typename... Args>
+static cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <int MODE>
 static cudaError_t run_decode(mlaq_cache* c, const DecodeParams& p, int grid_cta, cudaStream_t s) {
   const int smem = (int)sizeof(DecodeSmem);
@@ -1342,12 +1363,13 @@ static cudaError_t run_decode(mlaq_cache* c, const DecodeParams& p, int grid_cta
     if (dev >= 0 && dev < kMaxDevices) attr_done[dev] = true;
   }
   cudaEvent_t* ev = nullptr;
-  if (c->timing_events && c->timing_n < c->timing_max) {
-    ev = reinterpret_cast<cudaEvent_t*>(c->timing_events) + 2 * c->timing_n;
-    cudaEventRecord(ev[0], s);
+  if (c->timing_events && c->timing_n < c->timing_max)
+    ev = reinterpret_cast<cudaEvent_t*>(c->timing_events) + 2 * c->timing_n;  // ev[0] precedes the plan
+  cudaError_t e = launch_pdl(decode_kernel<MODE>, dim3(p.HB, grid_cta), dim3(kThreads), smem, s, p);
+  if (e == cudaSuccess) {
+    const int units = p.B * p.HB * 8;
+    e = launch_pdl(combine_kernel, dim3(max(1, min(units, 2 * c->decode_ctas))), dim3(128), 0, s, p);
   }
-  decode_kernel<MODE><<<dim3(p.HB, grid_cta), kThreads, smem, s>>>(p);
-  cudaError_t e = cudaGetLastError();
   if (ev) {
     cudaEventRecord(ev[1], s);
     c->timing_n++;
@@ -1378,7 +1400,6 @@ cudaError_t launch_decode(mlaq_cache* c, const uint16_t* q_latent, const uint16_
   p.item_start = reinterpret_cast<const int*>(ws + lay.item_start);
   p.cta_item_start = reinterpret_cast<const int*>(ws + lay.cta_item_start);
   p.cta_first = reinterpret_cast<const Item*>(ws + lay.cta_first);
-  p.counters = reinterpret_cast<int*>(ws + lay.counters);
   p.o_part = reinterpret_cast<__half*>(ws + lay.o_part);
   p.lse_part = reinterpret_cast<float*>(ws + lay.lse_part);
   p.out = out;
@@ -1404,12 +1425,13 @@ cudaError_t launch_decode(mlaq_cache* c, const uint16_t* q_latent, const uint16_
       if (dev >= 0 && dev < kMaxDevices) plan_attr_done[dev] = true;
     }
   }
-  plan_kernel<<<1, 1024, plan_smem_bytes(B, G), s>>>(p, c->mode, G, reinterpret_cast<Item*>(ws + lay.items),
-                                                     reinterpret_cast<int*>(ws + lay.item_start),
-                                                     reinterpret_cast<int*>(ws + lay.cta_item_start),
-                                                     reinterpret_cast<Item*>(ws + lay.cta_first),
-                                                     reinterpret_cast<int*>(ws + kWsNumItems));
-  cudaError_t e = cudaGetLastError();
+  // timed (mlaq_timing_enable): plan + decode + combine
+  if (c->timing_events && c->timing_n < c->timing_max)
+    cudaEventRecord(reinterpret_cast<cudaEvent_t*>(c->timing_events)[2 * c->timing_n], s);
+  cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(1024), plan_smem_bytes(B, G), s, p, (int)c->mode, G,
+                             reinterpret_cast<Item*>(ws + lay.items), reinterpret_cast<int*>(ws + lay.item_start),
+                             reinterpret_cast<int*>(ws + lay.cta_item_start),
+                             reinterpret_cast<Item*>(ws + lay.cta_first), reinterpret_cast<int*>(ws + kWsNumItems));
   if (e != cudaSuccess) return e;
   if (c->mode == MLAQ_C4R4) return run_decode<MLAQ_C4R4>(c, p, G, s);
   if (c->mode == MLAQ_C2R4) return run_decode<MLAQ_C2R4>(c, p, G, s);

@@ -62,7 +62,7 @@ inline size_t max_partial_rows(int max_seqs, int max_heads) {
 }
 
 struct WsLayout {
-  size_t items, item_start, cta_first, cta_item_start, counters, lse_part, o_part, total;
+  size_t items, item_start, cta_first, cta_item_start, lse_part, o_part, total;
 };
 inline WsLayout ws_layout(int max_seqs, int max_heads) {
   auto al = [](size_t x) { return (x + 255) / 256 * 256; };
@@ -72,7 +72,6 @@ inline WsLayout ws_layout(int max_seqs, int max_heads) {
   L.item_start = off;     off += al(((size_t)max_seqs + 1) * 4);
   L.cta_first = off;      off += al(((size_t)kMaxPlanCtas + 1) * sizeof(Item));
   L.cta_item_start = off; off += al(((size_t)kMaxPlanCtas + 1) * 4);
-  L.counters = off;       off += al((size_t)max_seqs * kMaxHeadBlocks * 4);
   const size_t rows = max_partial_rows(max_seqs, max_heads);
   L.lse_part = off;       off += al(rows * 4);
   L.o_part = off;         off += rows * kDL * 2;  // fp16 partial outputs
@@ -130,6 +129,10 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
+// Programmatic dependent launch: wait for the grid this one depends on (a
+// no-op when launched without the attribute), and let the next grid launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
