@@ -53,7 +53,7 @@ int mlaq_cache_create(mlaq_cache** out, int mode, int32_t num_pages, int32_t max
   *out = nullptr;
   if (!valid_mode(mode)) return MLAQ_ERR_MODE;
   if (num_pages <= 0 || max_seqs <= 0 || max_seqs > kMaxSeqs || max_pages_per_seq <= 0 || max_heads < 16 ||
-      max_heads > 128 || max_heads % 16)
+      max_heads > 128 || max_heads % 16 || !plan_cost_fits(max_seqs, max_pages_per_seq))
     return MLAQ_ERR_SHAPE;
   if (!codes || !workspace || (mode != MLAQ_BF16 && (!meta || !ring))) return MLAQ_ERR_NULL;
   if (!aligned16(codes) || !aligned16(workspace) || (mode != MLAQ_BF16 && (!aligned16(meta) || !aligned16(ring))))
@@ -132,6 +132,7 @@ int mlaq_decode_noalloc(int mode, const void* codes, const void* meta, const voi
   if (!codes || !q_latent || !q_rope || !page_table || !seq_lens || !out_latent || !lse) return MLAQ_ERR_NULL;
   if (mode != MLAQ_BF16 && (!meta || !ring)) return MLAQ_ERR_NULL;
   if (num_pages <= 0 || max_pages_per_seq <= 0) return MLAQ_ERR_SHAPE;
+  if (B <= 0 || !plan_cost_fits(B, max_pages_per_seq)) return MLAQ_ERR_SHAPE;
   if (B <= 0 || B > kMaxSeqs || H < 16 || H > 128 || H % 16) return MLAQ_ERR_SHAPE;
   if (!aligned16(codes) || !aligned16(q_latent) || !aligned16(q_rope) || !aligned16(out_latent) ||
       (mode != MLAQ_BF16 && (!aligned16(meta) || !aligned16(ring))))

@@ -109,18 +109,25 @@ __device__ __forceinline__ int seq_units(int mode, int L) {
   const int pages = L > kRing ? (L - kRecent + kPage - 1) / kPage : 0;
   return ring_units(mode, L) + 4 * pages;
 }
-// Planning cost, in quarter steps: a packed or BF16-page step (16 tokens)
-// costs 4, a ring step 5 (its BF16 tile takes about 1.3x the time of a
-// packed one on GB300). cost_to_unit maps a cost offset inside a sequence,
-// snapped to a step boundary, back to its unit index.
-constexpr int kCostStep = 4, kCostRing = 5;
+// Planning cost, in eighths of a packed step (16 tokens), as measured on
+// GB300: a packed or BF16-page step costs 8, a ring step 13 (its BF16 tile
+// is unpacked at 16 tokens per barrier pair, packed halves at 32), and the
+// first ring unit of a sequence carries kItemCost more for the item switch
+// (query load and epilogue) of the CTA that starts the sequence.
+constexpr int kCostStep = 8, kCostRing = 13, kItemCost = 40;
+__device__ __forceinline__ int ring_cost(int R) { return R > 0 ? kItemCost + kCostRing * R : 0; }
+static_assert(4 * kCostStep <= kPlanCostPerPage && kItemCost + kCostRing * kRingChunks <= kPlanCostRingMax,
+              "planner cost bounds");
 __device__ __forceinline__ int seq_cost(int mode, int L) {
   const int R = ring_units(mode, L);
-  return kCostRing * R + kCostStep * (seq_units(mode, L) - R);
+  return ring_cost(R) + kCostStep * (seq_units(mode, L) - R);
 }
+// Unit index of a cost offset inside a sequence that lies on a unit boundary.
 __device__ __forceinline__ int cost_to_unit(int mode, int L, int x) {
   const int R = ring_units(mode, L);
-  return x < kCostRing * R ? x / kCostRing : R + (x - kCostRing * R) / kCostStep;
+  const int xr = ring_cost(R);
+  if (x >= xr) return R + (x - xr) / kCostStep;
+  return x < kItemCost + kCostRing ? 0 : (x - kItemCost) / kCostRing;
 }
 
 // ---------------------------------------------------------------------------
@@ -230,10 +237,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, in
     if (raw < U) {
       const int b = last_le(useq, 0, B, raw);
       const int R = ring_units(mode, clamp_len(p.seq_lens[b], p.max_tokens));
-      const int xr = kCostRing * R;
+      const int xr = ring_cost(R);
       int x = raw - useq[b];
       if (x < xr)
-        x = (x / kCostRing) * kCostRing;
+        x = x < kItemCost + kCostRing ? 0 : kItemCost + ((x - kItemCost) / kCostRing) * kCostRing;
       else
         x = xr + ((x - xr) / (mode == MLAQ_BF16 ? kCostStep : 4 * kCostStep)) *
                      (mode == MLAQ_BF16 ? kCostStep : 4 * kCostStep);

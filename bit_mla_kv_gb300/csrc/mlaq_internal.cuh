@@ -33,6 +33,7 @@ constexpr int kMetaPage = kPage * kMetaTok;  // 2304
 // Workspace layout (bytes from the workspace base).
 constexpr size_t kWsStatus = 0;          // int32 sticky status
 constexpr size_t kWsNumItems = 4;        // int32 number of work items of the last plan
+constexpr size_t kWsAppendDone = 8;      // uint32 CTAs of the running append that have finished
 constexpr int kMaxPlanCtas = 1024;       // decode CTA count never exceeds this
 constexpr int kMaxSeqs = 16384;          // sequences per call
 constexpr int kMaxHeadBlocks = 8;        // 128 heads / 16
@@ -53,6 +54,13 @@ struct __align__(16) Item {
   int b, u_lo, u_hi, cta;
   int L, pad0, pad1, pad2;  // L: the sequence's (clamped) length when the plan was made
 };
+
+// Upper bounds of the planner's per-sequence cost (32-bit prefix sums): per
+// page of a sequence, and for its ring plus item overhead.
+constexpr int kPlanCostPerPage = 32, kPlanCostRingMax = 160;
+inline bool plan_cost_fits(int max_seqs, int max_pages_per_seq) {
+  return (long long)max_seqs * ((long long)max_pages_per_seq * kPlanCostPerPage + kPlanCostRingMax) < 0x7fffffffLL;
+}
 
 // Items: at most one per sequence plus one per CTA boundary inside a sequence.
 inline size_t max_items_for(int max_seqs) { return (size_t)max_seqs + kMaxPlanCtas + 1; }
