@@ -361,7 +361,7 @@ def run_mlaq(args, ws, rank, local):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_s * 1e3},
-        "gpu_launches": 5 * K,
+        "gpu_launches": 4 * K,  # per step: append, plan, decode, combine
         "clocks": clocks,
         "impl": "mlaq",
     }
