@@ -45,7 +45,6 @@ constexpr int kStages = MLAQ_STAGES;
 constexpr int kT = 16;                                // tokens per step
 constexpr int kRingChunks = (kRing + kT - 1) / kT;    // 9
 constexpr int kStageBytes = kPage * 288 + kMetaPage;  // 20736: max(C4R4 page + meta, 16 BF16 tokens)
-constexpr int kSpStride = 52;  // floats per row of partial scores [h][t] (32 tokens; 52 = 20 mod 32)
 constexpr int kPStride = 40;   // halfs per row of P [h][t] (32 tokens; 80-byte rows for ldmatrix)
 constexpr uint64_t kWaitLimit = 200000000ull;  // 200 ms per bounded wait
 constexpr int kMaxDevices = 64;
@@ -53,13 +52,17 @@ template <bool B>
 struct BoolC {
   static constexpr bool value = B;
 };
+// MLAQ_TC_AGG=1 (default): aggregation on tcgen05 with O^T in TMEM, whole
+// valid pages as one step. MLAQ_TC_AGG=0: register MMAs, half-page steps.
 #ifndef MLAQ_TC_AGG
-#define MLAQ_TC_AGG 0
+#define MLAQ_TC_AGG 1
 #endif
+// floats per row of partial scores [h][t]: 32 tokens (52 = 20 mod 32), or 64 with tcgen05 page steps
+constexpr int kSpStride = MLAQ_TC_AGG ? 68 : 52;
 #if MLAQ_TC_AGG
 // Aggregation on tcgen05 (MLAQ_TC_AGG): O^T[channel][head] accumulates in TMEM.
 constexpr int kAggBufs = 2;      // A (content) / P^T step buffers in flight
-constexpr int kTmemCols = 128;   // O^T: 4 blocks x 16 heads; A: 2 buffers x 4 blocks x 8 columns
+constexpr int kTmemCols = 256;   // O^T: 4 blocks x 16 heads; A: 4 sub-steps x 4 blocks x 8 columns
 constexpr int kTmemA = 64;       // first column of the A step buffers
 #endif
 
@@ -95,6 +98,7 @@ struct __align__(16) DecodeSmem {
   uint64_t full[kStages];
 #if MLAQ_TC_AGG
   __align__(128) uint8_t pt[kAggBufs][512];  // P^T B operand: 16 heads x 16 tokens, 8x8 core matrices
+  __align__(128) uint8_t ptp[4][512];        // P^T of the four sub-steps of a page step
   uint64_t agg_done[kAggBufs];
   uint32_t tmem_base;
   int rescale_flag[kWarps];
@@ -787,8 +791,10 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
         // content tile -> TMEM A step buffer (lanes = channels, columns = token pairs)
         const int ab = agg_ctr % kAggBufs;
         bool agg_ok = true;
-        if (agg_ctr >= kAggBufs)  // MMAs that last read this buffer must be complete
-          agg_ok = mbar_wait_bounded(&sm.agg_done[ab], ((agg_ctr / kAggBufs) - 1) & 1, kWaitLimit);
+        if (agg_ctr > 0) {  // every earlier aggregation MMA is complete (a page step reads all A columns)
+          const int lp = agg_ctr - 1;
+          agg_ok = mbar_wait_bounded(&sm.agg_done[lp % kAggBufs], (lp / kAggBufs) & 1, kWaitLimit);
+        }
         tc_fence_after();
 #pragma unroll
         for (int j = 0; j < 2; ++j)
@@ -1122,6 +1128,246 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
         return false;
       };
 #endif
+#if MLAQ_TC_AGG
+      // A whole packed page (64 tokens, all valid) under one pair of
+      // barriers. The four 16-token sub-steps store their dequantized,
+      // transposed content tiles in TMEM (A operand, lanes = channels) and
+      // publish partial scores; after the softmax of all 64 tokens each warp
+      // issues four tcgen05 MMAs (its 128-channel block) that accumulate
+      // O^T += V^T P^T asynchronously.
+      auto page_body = [&]() -> bool {
+        bool agg_ok = true;
+        if (agg_ctr > 0) {  // every earlier aggregation MMA has read its TMEM/smem operands
+          const int lp = agg_ctr - 1;
+          agg_ok = mbar_wait_bounded(&sm.agg_done[lp % kAggBufs], (lp / kAggBufs) & 1, kWaitLimit);
+        }
+        tc_fence_after();
+        const uint8_t* mtab = st + page_code_bytes(MODE);
+#pragma unroll 1
+        for (int sub = 0; sub < 4; ++sub) {
+          const int lr = 16 * sub + r;
+          uint32_t mx[3], my[3];
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            const int gg = j < 2 ? 2 * w + j : 8;
+            mx[j] = *reinterpret_cast<const uint32_t*>(mtab + lr * kMetaTok + 4 * gg);
+            my[j] = *reinterpret_cast<const uint32_t*>(mtab + (lr + 8) * kMetaTok + 4 * gg);
+          }
+          uint32_t ch[2][4][4];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int gg = 2 * w + j;
+            if constexpr (CBITS == 4) {
+              const uint2 wx = *reinterpret_cast<const uint2*>(st + lr * CB + gg * GBYTES + 8 * i);
+              const uint2 wy = *reinterpret_cast<const uint2*>(st + (lr + 8) * CB + gg * GBYTES + 8 * i);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t ax = (kk >> 1) ? wx.y : wx.x, ay = (kk >> 1) ? wy.y : wy.x;
+                const uint32_t ax8 = ax >> 8, ay8 = ay >> 8;
+                const int p0 = 2 * (kk & 1);
+                ch[j][kk][0] = int4_pos(ax, ax8, p0);
+                ch[j][kk][1] = int4_pos(ay, ay8, p0);
+                ch[j][kk][2] = int4_pos(ax, ax8, p0 + 1);
+                ch[j][kk][3] = int4_pos(ay, ay8, p0 + 1);
+              }
+            } else {
+              const uint32_t ax = *reinterpret_cast<const uint32_t*>(st + lr * CB + gg * GBYTES + 4 * i);
+              const uint32_t ay = *reinterpret_cast<const uint32_t*>(st + (lr + 8) * CB + gg * GBYTES + 4 * i);
+              const uint32_t ax8 = ax >> 8, ay8 = ay >> 8;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                ch[j][kk][0] = int2_pos(ax, ax8, 2 * kk);
+                ch[j][kk][1] = int2_pos(ay, ay8, 2 * kk);
+                ch[j][kk][2] = int2_pos(ax, ax8, 2 * kk + 1);
+                ch[j][kk][3] = int2_pos(ay, ay8, 2 * kk + 1);
+              }
+            }
+          }
+          uint32_t rf[4];
+          {
+            uint32_t ax = *reinterpret_cast<const uint32_t*>(st + lr * CB + ROPE_OFF + 4 * (2 * w + (i >> 1)));
+            uint32_t ay = *reinterpret_cast<const uint32_t*>(st + (lr + 8) * CB + ROPE_OFF + 4 * (2 * w + (i >> 1)));
+            if (i & 1) {
+              ax >>= 8;
+              ay >>= 8;
+            }
+            rf[0] = int4_pos(ax, 0u, 0);
+            rf[1] = int4_pos(ay, 0u, 0);
+            rf[2] = int4_pos(ax, 0u, 1);
+            rf[3] = int4_pos(ay, 0u, 1);
+          }
+          float sacc[2][4];
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[hb][e] = 0.f;
+          {
+            uint32_t a[4];
+            const uint32_t mnx = (i == 0) ? mx[0] : (i == 1) ? mx[1] : mx[2];
+            const uint32_t mny = (i == 0) ? my[0] : (i == 1) ? my[1] : my[2];
+            a[0] = (i < 3) ? __byte_perm(mnx, 0, 0x3232) : 0u;
+            a[1] = (i < 3) ? __byte_perm(mny, 0, 0x3232) : 0u;
+            a[2] = 0u;
+            a[3] = 0u;
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) mma16816(sacc[hb], a, kmn[hb], 0u);
+          }
+          {
+            float d0[2][4], d1[2][4], d2[2][4];
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) d0[hb][e] = d1[hb][e] = d2[hb][e] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              mma16816(d0[0], ch[0][kk], qf[0][kk][0][0], qf[0][kk][0][1]);
+              mma16816(d1[0], ch[1][kk], qf[1][kk][0][0], qf[1][kk][0][1]);
+              mma16816(d0[1], ch[0][kk], qf[0][kk][1][0], qf[0][kk][1][1]);
+              mma16816(d1[1], ch[1][kk], qf[1][kk][1][0], qf[1][kk][1][1]);
+            }
+            mma16816(d2[0], rf, qr[0][0], qr[0][1]);
+            mma16816(d2[1], rf, qr[1][0], qr[1][1]);
+            float sxv[3], syv[3];
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+              sxv[j] = __half2float(__ushort_as_half((unsigned short)(mx[j] & 0xffffu)));
+              syv[j] = __half2float(__ushort_as_half((unsigned short)(my[j] & 0xffffu)));
+            }
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+              sacc[hb][0] = fmaf(sxv[2], d2[hb][0], fmaf(sxv[1], d1[hb][0], fmaf(sxv[0], d0[hb][0], sacc[hb][0])));
+              sacc[hb][1] = fmaf(sxv[2], d2[hb][1], fmaf(sxv[1], d1[hb][1], fmaf(sxv[0], d0[hb][1], sacc[hb][1])));
+              sacc[hb][2] = fmaf(syv[2], d2[hb][2], fmaf(syv[1], d1[hb][2], fmaf(syv[0], d0[hb][2], sacc[hb][2])));
+              sacc[hb][3] = fmaf(syv[2], d2[hb][3], fmaf(syv[1], d1[hb][3], fmaf(syv[0], d0[hb][3], sacc[hb][3])));
+            }
+          }
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            const int h = 8 * hb + 2 * i;
+            const int t = 16 * sub + r;
+            sm.sp[w][h][t] = sacc[hb][0];
+            sm.sp[w][h + 1][t] = sacc[hb][1];
+            sm.sp[w][h][t + 8] = sacc[hb][2];
+            sm.sp[w][h + 1][t + 8] = sacc[hb][3];
+          }
+          // dequantize, transpose, and store the sub-step's A tile in TMEM
+          // (lanes = channels, columns = token pairs)
+          uint32_t vv[2][16];  // [kk & 1][column block blk = 2j + kk / 2][4 registers]
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const __half2 s2x = __low2half2(u32_as_h2(mx[j])), m2x = __high2half2(u32_as_h2(mx[j]));
+            const __half2 s2y = __low2half2(u32_as_h2(my[j])), m2y = __high2half2(u32_as_h2(my[j]));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const int blk = 2 * j + (kk >> 1);
+              uint32_t* v = &vv[kk & 1][4 * blk];
+              v[0] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][0]), s2x, m2x)));
+              v[1] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][1]), s2y, m2y)));
+              v[2] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][2]), s2x, m2x)));
+              v[3] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][3]), s2y, m2y)));
+            }
+          }
+#pragma unroll
+          for (int k2 = 0; k2 < 2; ++k2)
+            tmem_st_16x256b_x4(tmem + ((uint32_t)(32 * w + 16 * k2) << 16) + (uint32_t)(kTmemA + 32 * sub), vv[k2]);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        // barrier 1: partial scores and A tiles complete; agrees on a timed-out wait
+        if (named_bar_or(1, kThreads, !(ok && agg_ok))) return true;
+        if (tid == 0) producer_advance<MODE>(p, sm, pc, i1);
+        // online softmax for head hh, tokens tq .. tq + 7 (sub-step tq / 16)
+        {
+          const int tq = 8 * (lane & 7);
+          float x[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) x[u] = 0.f;
+#pragma unroll
+          for (int ww = 0; ww < kWarps; ++ww) {
+            const float4 v0 = *reinterpret_cast<const float4*>(&sm.sp[ww][hh][tq]);
+            const float4 v1 = *reinterpret_cast<const float4*>(&sm.sp[ww][hh][tq + 4]);
+            x[0] += v0.x;
+            x[1] += v0.y;
+            x[2] += v0.z;
+            x[3] += v0.w;
+            x[4] += v1.x;
+            x[5] += v1.y;
+            x[6] += v1.z;
+            x[7] += v1.w;
+          }
+          float xm = -INFINITY;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            x[u] *= p.scale_log2;
+            xm = fmaxf(xm, x[u]);
+          }
+          float alpha = 1.f;
+          if (__any_sync(0xffffffffu, xm > m_run + 8.f)) {
+            float tmax = xm;
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+            const bool upd = tmax > m_run + 8.f;
+            alpha = upd ? ex2(m_run - tmax) : 1.f;
+            m_run = upd ? tmax : m_run;
+          }
+          float psum = 0.f;
+          const int sub = tq >> 4;
+#pragma unroll
+          for (int u = 0; u < 8; u += 2) {
+            const float pa = ex2(x[u] - m_run), pb = ex2(x[u + 1] - m_run);
+            psum += pa + pb;
+            const int t = (tq & 15) + u;              // token pair t, t + 1 of the sub-step
+            const int kp = t < 8 ? 2 * t : 2 * t - 14;  // their K index in the TMEM A columns
+            const int off = (hh >> 3) * 256 + (kp >> 3) * 128 + (hh & 7) * 16 + (kp & 7) * 2;
+            *reinterpret_cast<__half2*>(&sm.ptp[sub][off]) = __floats2half2_rn(pa, pb);
+          }
+          l_run = l_run * alpha + psum;
+          fence_view_async_shared();
+          const bool any_rs = __any_sync(0xffffffffu, alpha != 1.f);
+          if (lane == 0) sm.rescale_flag[w] = any_rs;
+          if ((lane & 7) == 0) sm.alpha[hh] = alpha;
+        }
+        named_bar_sync(2, kThreads);
+        {
+          const bool need_rs = !item_first && (sm.rescale_flag[0] | sm.rescale_flag[1] | sm.rescale_flag[2] |
+                                               sm.rescale_flag[3]);
+          if (need_rs) {  // rare (lazy max): scale O^T columns by alpha[head]; no MMA is in flight
+            float al[16];
+#pragma unroll
+            for (int h = 0; h < 16; ++h) al[h] = sm.alpha[h];
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) {
+              uint32_t v[16];
+              const uint32_t ta = tmem + ((uint32_t)(32 * w) << 16) + (uint32_t)(16 * blk);
+              tmem_ld_32x32b_x16(ta, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int h = 0; h < 16; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * al[h]);
+              tmem_st_32x32b_x16(ta, v);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            named_bar_sync(3, kThreads);
+            tc_fence_after();
+          }
+          if (lane == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int sub = 0; sub < 4; ++sub) {
+              const uint64_t bdesc = umma_smem_desc(smem_u32(sm.ptp[sub]), 128, 256);
+              umma_f16_ts(tmem + (uint32_t)(16 * w), tmem + (uint32_t)(kTmemA + 32 * sub + 8 * w), bdesc,
+                          kAggIdesc, !item_first || sub > 0);
+            }
+            umma_commit(&sm.agg_done[agg_ctr % kAggBufs]);
+          }
+          __syncwarp();
+          item_first = false;
+          agg_ctr++;
+        }
+        return false;
+      };
+#endif
 #if !MLAQ_TC_AGG
       if constexpr (MODE != MLAQ_BF16) {
         // packed stage: all-valid halves take the 32-token body; the decision
@@ -1146,6 +1392,20 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
             g_fail = g - 1;
           }
           continue;
+        }
+      }
+#endif
+#if MLAQ_TC_AGG
+      if constexpr (MODE != MLAQ_BF16) {
+        if (packed) {
+          const int t0 = kPage * sref.idx;
+          if (!bad && t0 >= kSink && t0 + kPage <= L - kRecent) {  // CTA-uniform
+            if (page_body()) {
+              failed = true;
+              g_fail = g - 1;
+            }
+            continue;
+          }
         }
       }
 #endif

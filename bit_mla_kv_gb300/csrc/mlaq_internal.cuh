@@ -255,6 +255,16 @@ __device__ __forceinline__ void tmem_st_16x256b(uint32_t taddr, uint32_t r0, uin
                "r"(r3)
                : "memory");
 }
+// Four 16x256b tiles side by side (columns 0-7, 8-15, 16-23, 24-31): regs
+// 4k..4k+3 go to column block k in the x1 layout.
+__device__ __forceinline__ void tmem_st_16x256b_x4(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
 // 32 lanes x 32 bits x 16: thread t reads lane t, 16 consecutive columns
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&v)[16]) {
   asm volatile(
