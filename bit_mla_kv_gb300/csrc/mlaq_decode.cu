@@ -114,11 +114,11 @@ __device__ __forceinline__ int seq_units(int mode, int L) {
   return ring_units(mode, L) + 4 * pages;
 }
 // Planning cost, in eighths of a packed step (16 tokens), as measured on
-// GB300: a packed or BF16-page step costs 8, a ring step 13 (its BF16 tile
-// is unpacked at 16 tokens per barrier pair, packed halves at 32), and the
-// first ring unit of a sequence carries kItemCost more for the item switch
-// (query load and epilogue) of the CTA that starts the sequence.
-constexpr int kCostStep = 8, kCostRing = 13, kItemCost = 40;
+// GB300: a packed or BF16-page step costs 8; a ring step 19 (its BF16 tile
+// runs 16 tokens per barrier pair, packed pages 64: 3300 against 1370
+// cycles per 16 tokens); the first ring unit of a sequence carries kItemCost
+// more for the item switch (query load, epilogue) of the CTA that starts it.
+constexpr int kCostStep = 8, kCostRing = 19, kItemCost = 40;
 __device__ __forceinline__ int ring_cost(int R) { return R > 0 ? kItemCost + kCostRing * R : 0; }
 static_assert(4 * kCostStep <= kPlanCostPerPage && kItemCost + kCostRing * kRingChunks <= kPlanCostRingMax,
               "planner cost bounds");
@@ -521,7 +521,8 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
 #if MLAQ_TC_AGG
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  int agg_ctr = 0;  // aggregation steps issued by this CTA
+  int agg_ctr = 0;    // aggregation steps issued by this CTA
+  int page_ctr = -1;  // the last of them that was a page step (reads every A column)
   constexpr uint32_t kAggIdesc = umma_idesc_f16(128, 16);
 #endif
   ProdCursor pc;
@@ -791,9 +792,11 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
         // content tile -> TMEM A step buffer (lanes = channels, columns = token pairs)
         const int ab = agg_ctr % kAggBufs;
         bool agg_ok = true;
-        if (agg_ctr > 0) {  // every earlier aggregation MMA is complete (a page step reads all A columns)
-          const int lp = agg_ctr - 1;
-          agg_ok = mbar_wait_bounded(&sm.agg_done[lp % kAggBufs], (lp / kAggBufs) & 1, kWaitLimit);
+        {
+          // the MMAs that last read buffer ab (two steps back), or a later
+          // page step's, which read every A column, must be complete
+          const int lp = max(agg_ctr - kAggBufs, page_ctr);
+          if (lp >= 0) agg_ok = mbar_wait_bounded(&sm.agg_done[lp % kAggBufs], (lp / kAggBufs) & 1, kWaitLimit);
         }
         tc_fence_after();
 #pragma unroll
@@ -1363,6 +1366,7 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
           }
           __syncwarp();
           item_first = false;
+          page_ctr = agg_ctr;
           agg_ctr++;
         }
         return false;

@@ -57,7 +57,7 @@ struct __align__(16) Item {
 
 // Upper bounds of the planner's per-sequence cost (32-bit prefix sums): per
 // page of a sequence, and for its ring plus item overhead.
-constexpr int kPlanCostPerPage = 32, kPlanCostRingMax = 160;
+constexpr int kPlanCostPerPage = 32, kPlanCostRingMax = 224;
 inline bool plan_cost_fits(int max_seqs, int max_pages_per_seq) {
   return (long long)max_seqs * ((long long)max_pages_per_seq * kPlanCostPerPage + kPlanCostRingMax) < 0x7fffffffLL;
 }

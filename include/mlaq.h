@@ -107,7 +107,7 @@ int mlaq_buffer_sizes(int mode, int32_t num_pages, int32_t max_seqs, int32_t max
  * passed to each call; row b of a page table (and seq_lens[b]) is sequence
  * slot b, which also selects ring slot b. The handle is host memory; destroy
  * it with mlaq_cache_destroy. Queries the current device's SM count.
- * MLAQ_ERR_SHAPE also when max_seqs * (32 * max_pages_per_seq + 160) reaches
+ * MLAQ_ERR_SHAPE also when max_seqs * (32 * max_pages_per_seq + 224) reaches
  * 2^31 (the device planner's 32-bit cost sums). */
 int mlaq_cache_create(mlaq_cache** out, int mode, int32_t num_pages, int32_t max_seqs,
                       int32_t max_pages_per_seq, int32_t max_heads, void* codes, void* meta,

@@ -62,7 +62,7 @@ def test_host_argument_errors(lib):
     assert lib.mlaq_cache_create(ctypes.byref(out), 7, 1, 1, 1, 16, None, None, None, None, ctypes.c_size_t(0)) == -2
     assert lib.mlaq_cache_create(ctypes.byref(out), 0, 0, 1, 1, 16, None, None, None, None, ctypes.c_size_t(0)) == -3
     assert lib.mlaq_cache_create(ctypes.byref(out), 0, 1, 1, 1, 16, None, None, None, None, ctypes.c_size_t(0)) == -1
-    # plan cost sums would overflow 32 bits: 16384 * (32 * 5000 + 160) >= 2^31
+    # plan cost sums would overflow 32 bits: 16384 * (32 * 5000 + 224) >= 2^31
     assert lib.mlaq_cache_create(ctypes.byref(out), 0, 1, 16384, 5000, 16, None, None, None, None, ctypes.c_size_t(0)) == -3
     buf = ctypes.create_string_buffer(64)
     addr = (ctypes.addressof(buf) + 15) // 16 * 16
