@@ -201,10 +201,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, in
   pdl_launch_dependents();  // the decode grid may launch and wait for this one
   const int tid = threadIdx.x;
   const int B = p.B;
-  int* useq = plan_smem;
-  int* sitem = useq + (B + 1);
-  int* bnd = sitem + (B + 1);
-  int* ne = bnd + (G + 1);
+  int* useq = plan_smem;       // [B + 1] cost prefix
+  int* sfc = useq + (B + 1);    // [B + 1] first item << 10 | first CTA of each sequence
+  int* bnd = sfc + (B + 1);     // [G + 1] CTA boundaries (cost)
+  int* ne = bnd + (G + 1);      // [G + 1] non-empty CTAs below c
   // A: units per sequence -> useq (exclusive prefix); reset the merge
   //    empty sequences get out = 0, lse = -inf.
   if (tid == 0) carry_s = 0;
@@ -262,19 +262,18 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, in
     if (c <= G) ne[c] = ex;
     __syncthreads();
   }
-  // D: items per sequence (one per non-empty CTA overlapping it), emission
+  // D: item counts per sequence (one per non-empty CTA overlapping it) ->
+  //    first item of each sequence (exclusive prefix)
   if (tid == 0) carry_s = 0;
   __syncthreads();
   for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + tid;
-    int cnt = 0, c_lo = 0, c_hi = -1, u0 = 0, u1 = 0, Lb = 0;
+    int cnt = 0, c_lo = 0;
     if (b < B) {
-      Lb = clamp_len(p.seq_lens[b], p.max_tokens);
-      u0 = useq[b];
-      u1 = useq[b + 1];
+      const int u0 = useq[b], u1 = useq[b + 1];
       if (u1 > u0) {
         c_lo = last_le(bnd, 0, G - 1, u0);
-        c_hi = last_le(bnd, 0, G - 1, u1 - 1);
+        const int c_hi = last_le(bnd, 0, G - 1, u1 - 1);
         cnt = ne[c_hi + 1] - ne[c_lo];
       }
     }
@@ -282,13 +281,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, in
     const int ex = block_excl_scan(cnt, red, &tot);
     const int carry = carry_s;
     if (b < B) {
-      int k = carry + ex;
-      item_start[b] = k;
-      sitem[b] = k;
-      for (int c = c_lo; c <= c_hi; ++c)
-        if (bnd[c] < bnd[c + 1])
-          items[k++] = Item{b, cost_to_unit(mode, Lb, max(bnd[c], u0) - u0),
-                            cost_to_unit(mode, Lb, min(bnd[c + 1], u1) - u0), c, Lb, 0, 0, 0};
+      item_start[b] = carry + ex;
+      sfc[b] = ((carry + ex) << 10) | c_lo;  // items < 2^21, CTAs < 2^10
     }
     __syncthreads();
     if (tid == 0) carry_s = carry + tot;
@@ -299,25 +293,36 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, in
     item_start[B] = n;
     *num_items = n;
   }
-  // E: first item of every CTA. Items are ordered by unit position; the first
-  // item at or after unit bnd[c] (in sequence bs) is the first item of bs plus
-  // the non-empty CTAs between the first CTA of bs and c. An empty CTA gets
-  // the same value as the next non-empty one, so its item range is empty.
+  // E: one thread per CTA writes its items. Items are ordered by sequence,
+  // then CTA: the item of (sequence b, CTA c) is sitem[b] plus the non-empty
+  // CTAs between the first CTA of b and c. An empty CTA gets the index of the
+  // next item, so its item range is empty.
   for (int c = tid; c <= G; c += blockDim.x) {
     int v = n;
     if (bnd[c] < U) {
       const int bs = last_le(useq, 0, B, bnd[c]);
-      const int c_lo = last_le(bnd, 0, G - 1, useq[bs]);
-      v = sitem[bs] + ne[c] - ne[c_lo];
+      v = (sfc[bs] >> 10) + ne[c] - ne[sfc[bs] & 1023];
+      if (c < G && bnd[c] < bnd[c + 1]) {
+        int k = v;
+        for (int b = bs; b < B && useq[b] < bnd[c + 1]; ++b) {
+          const int u0 = useq[b], u1 = useq[b + 1];
+          if (u1 == u0) continue;  // empty sequence: no item
+          const int Lb = clamp_len(p.seq_lens[b], p.max_tokens);
+          const Item it{b, cost_to_unit(mode, Lb, max(bnd[c], u0) - u0), cost_to_unit(mode, Lb, min(bnd[c + 1], u1) - u0),
+                        c, Lb, 0, 0, 0};
+          items[k] = it;
+          if (k == v) {
+            // the CTA's first item, with the page of its first stage, so that
+            // the decode CTA can issue its first copy after a single load
+            Item f = it;
+            f.pad0 = first_stage_page(p, mode, f);
+            cta_first[c] = f;
+          }
+          ++k;
+        }
+      }
     }
     cta_item_start[c] = v;
-    // the CTA's first item, with the page of its first stage, so that the
-    // decode CTA can issue its first copy after a single load
-    if (c < G && v < n) {
-      Item f = items[v];
-      f.pad0 = first_stage_page(p, mode, f);
-      cta_first[c] = f;
-    }
   }
 }
 
