@@ -91,6 +91,26 @@ def test_decode_more_heads(H):
         assert_close_out(out[b], lse[b], ro, rl, f"H={H} seq {b}")
 
 
+@pytest.mark.parametrize("mode", ["C4R4", "C2R4", "BF16"])
+def test_decode_running_max_rescale(mode):
+    # Later tokens carry larger latents, so the running max of every head
+    # rises by far more than the lazy-rescale threshold partway through each
+    # sequence: the accumulated output (TMEM or registers) must be rescaled
+    # mid-item, in full-page and 16-token steps and across splits.
+    case = Case(mode, [700, 3000, 5000], 16, seed=22)
+    for b, L in enumerate(case.seq_lens):
+        a = int(case.cu[b])
+        for lo, f in ((L // 3, 3.0), (2 * L // 3, 6.0)):
+            case.c[a + lo:a + L] = (case.c[a + lo:a + L].float() * f).to(torch.bfloat16)
+    case.build()
+    for ctas in (1, 300):
+        case.cache.set_decode_ctas(ctas)
+        out, lse = case.decode()
+        for b in range(case.B):
+            ro, rl = case.oracle_seq(b)
+            assert_close_out(out[b], lse[b], ro, rl, f"{mode} ctas={ctas} seq {b}")
+
+
 def test_split_invariance():
     case = Case("C4R4", [3000, 9000, 133, 640], 16, seed=15)
     case.build()
