@@ -135,7 +135,7 @@ __device__ __forceinline__ int cost_to_unit(int mode, int L, int x) {
 }
 
 // ---------------------------------------------------------------------------
-// Block-wide exclusive scan of one int per thread (blockDim.x == 1024).
+// Block-wide exclusive scan of one int per thread (blockDim.x a multiple of 32).
 __device__ int block_excl_scan(int v, int* red, int* total) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   int x = v;
@@ -148,7 +148,7 @@ __device__ int block_excl_scan(int v, int* red, int* total) {
   if (lane == 31) red[wid] = x;
   __syncthreads();
   if (wid == 0) {
-    int y = red[lane];
+    int y = lane < (int)(blockDim.x >> 5) ? red[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       int u = __shfl_up_sync(0xffffffffu, y, o);
@@ -1704,7 +1704,10 @@ cudaError_t launch_decode(mlaq_cache* c, const uint16_t* q_latent, const uint16_
   // timed (mlaq_timing_enable): plan + decode + combine
   if (c->timing_events && c->timing_n < c->timing_max)
     cudaEventRecord(reinterpret_cast<cudaEvent_t*>(c->timing_events)[2 * c->timing_n], s);
-  cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(1024), plan_smem_bytes(B, G), s, p, (int)c->mode, G,
+  // one thread per sequence or CTA boundary (pass C scans G + 1 values in one
+  // pass), in whole warps: small batches synchronise fewer warps
+  const int plan_threads = min(1024, (max(B, G + 1) + 31) / 32 * 32);
+  cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(plan_threads), plan_smem_bytes(B, G), s, p, (int)c->mode, G,
                              reinterpret_cast<Item*>(ws + lay.items), reinterpret_cast<int*>(ws + lay.item_start),
                              reinterpret_cast<int*>(ws + lay.cta_item_start),
                              reinterpret_cast<Item*>(ws + lay.cta_first), reinterpret_cast<int*>(ws + kWsNumItems));
