@@ -319,6 +319,10 @@ def run_mlaq(args, ws, rank, local):
     barrier(ws)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
+    # The host enqueues every step (pinned inputs in, out/lse back) without
+    # waiting for the previous one, as a serving loop would; the copies run in
+    # stream order with the kernels, and the time ends when the last step's
+    # result is on the host.
     for j in range(K):
         d_ql.copy_(h_ql, non_blocking=True)
         d_qr.copy_(h_qr, non_blocking=True)
@@ -328,7 +332,7 @@ def run_mlaq(args, ws, rank, local):
         cache.decode(d_ql, d_qr, inp["pt"], seq, W.SOFTMAX_SCALE, out=out, lse=lse)
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
-        torch.cuda.synchronize()
+    torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / K
     barrier(ws)
     e2e_s = max_over_ranks(e2e_s, ws, device)
@@ -360,7 +364,10 @@ def run_mlaq(args, ws, rank, local):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_s * 1e3},
+                "ms_per_step": e2e_s * 1e3,
+                "how": "host wall time over K steps; each step copies its inputs from pinned host memory, "
+                       "runs mlaq_append + mlaq_decode and copies out/lse back, all in stream order; one "
+                       "synchronize at the end"},
         "gpu_launches": 4 * K,  # per step: append, plan, decode, combine
         "clocks": clocks,
         "impl": "mlaq",
