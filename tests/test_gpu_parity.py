@@ -194,6 +194,22 @@ def test_full_size_sampled(name, sample):
         assert_close_out(out[b], lse[b], ro, rl, f"{name} seq {b}")
 
 
+@pytest.mark.parametrize("mode", ["C4R4", "BF16"])
+def test_many_short_sequences(mode):
+    """A large batch of short and empty sequences: the planner's multi-pass
+    scans, CTAs that hold many whole sequences, and sequences split across CTA
+    boundaries all at once; every sequence is checked."""
+    rng = np.random.default_rng(23)
+    lens = [int(x) for x in rng.choice([0, 1, 4, 5, 64, 65, 131, 133, 200, 300, 700], size=3000)]
+    case = Case(mode, lens, 16, seed=23, gen_device="cuda")
+    case.build()
+    out, lse = case.decode()
+    assert case.cache.device_status() == 0
+    for b in range(case.B):
+        ro, rl = case.oracle_seq(b)
+        assert_close_out(out[b], lse[b], ro, rl, f"{mode} seq {b} L={lens[b]}")
+
+
 def test_serving_loop_sampled():
     """Serving loop at full size: B=128, H=16, L0~U[2K,16K], 256 steps of
     mlaq_append (one token per sequence) + mlaq_decode. Appended codes are
