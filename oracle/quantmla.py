@@ -15,7 +15,7 @@ Quantization for Low-Bit MLA KV Caching", arXiv 2609.36760):
   [TDH]  tokendh.com article -- section "从实验室到实际部署" (sink/recent
          protection zone, 27.9% / 3.59x persistent cache at 128K).
 
-Readings taken where the pages are silent (each also listed in the design doc):
+Readings taken where the pages are silent:
   R1  quantizer arithmetic: mn = min(x); s32 = (max(x) - mn) / (2^b - 1) in
       IEEE fp32; the stored metadata are s = fp16_rn(s32), m = fp16_rn(mn);
       codes use the STORED (s, m): q = clamp(rint_even((x - m) / s), 0, 2^b-1)
