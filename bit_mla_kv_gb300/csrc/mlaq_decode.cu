@@ -1143,7 +1143,10 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
       // publish partial scores; after the softmax of all 64 tokens each warp
       // issues four tcgen05 MMAs (its 128-channel block) that accumulate
       // O^T += V^T P^T asynchronously.
-      auto page_body = [&]() -> bool {
+      // MASKED: rows outside the packed range [4, L - 128) contribute nothing
+      // (zero scale and min, score -inf); the first and last pages of a range.
+      auto page_body = [&](auto masked_c) -> bool {
+        constexpr bool MASKED = decltype(masked_c)::value;
         bool agg_ok = true;
         if (agg_ctr > 0) {  // every earlier aggregation MMA has read its TMEM/smem operands
           const int lp = agg_ctr - 1;
@@ -1154,12 +1157,20 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
 #pragma unroll 1
         for (int sub = 0; sub < 4; ++sub) {
           const int lr = 16 * sub + r;
+          bool v0 = true, v1 = true;
+          if constexpr (MASKED) {
+            const int t = kPage * sref.idx + lr;
+            v0 = (t >= kSink) & (t < L - kRecent);
+            v1 = (t + 8 >= kSink) & (t + 8 < L - kRecent);
+          }
           uint32_t mx[3], my[3];
 #pragma unroll
           for (int j = 0; j < 3; ++j) {
             const int gg = j < 2 ? 2 * w + j : 8;
-            mx[j] = *reinterpret_cast<const uint32_t*>(mtab + lr * kMetaTok + 4 * gg);
-            my[j] = *reinterpret_cast<const uint32_t*>(mtab + (lr + 8) * kMetaTok + 4 * gg);
+            const uint32_t mxr = *reinterpret_cast<const uint32_t*>(mtab + lr * kMetaTok + 4 * gg);
+            const uint32_t myr = *reinterpret_cast<const uint32_t*>(mtab + (lr + 8) * kMetaTok + 4 * gg);
+            mx[j] = v0 ? mxr : 0u;
+            my[j] = v1 ? myr : 0u;
           }
           uint32_t ch[2][4][4];
 #pragma unroll
@@ -1306,7 +1317,12 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
           float xm = -INFINITY;
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            x[u] *= p.scale_log2;
+            bool valid = true;
+            if constexpr (MASKED) {
+              const int t = kPage * sref.idx + tq + u;
+              valid = (t >= kSink) & (t < L - kRecent);
+            }
+            x[u] = valid ? x[u] * p.scale_log2 : -INFINITY;
             xm = fmaxf(xm, x[u]);
           }
           float alpha = 1.f;
@@ -1321,9 +1337,10 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
           }
           float psum = 0.f;
           const int sub = tq >> 4;
+          const float mref = (MASKED && m_run == -INFINITY) ? 0.f : m_run;  // nothing valid yet: p = 0
 #pragma unroll
           for (int u = 0; u < 8; u += 2) {
-            const float pa = ex2(x[u] - m_run), pb = ex2(x[u + 1] - m_run);
+            const float pa = ex2(x[u] - mref), pb = ex2(x[u + 1] - mref);
             psum += pa + pb;
             const int t = (tq & 15) + u;              // token pair t, t + 1 of the sub-step
             const int kp = t < 8 ? 2 * t : 2 * t - 14;  // their K index in the TMEM A columns
@@ -1408,8 +1425,9 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
       if constexpr (MODE != MLAQ_BF16) {
         if (packed) {
           const int t0 = kPage * sref.idx;
-          if (!bad && t0 >= kSink && t0 + kPage <= L - kRecent) {  // CTA-uniform
-            if (page_body()) {
+          if (!bad) {  // CTA-uniform
+            const bool full = t0 >= kSink && t0 + kPage <= L - kRecent;
+            if (full ? page_body(BoolC<false>{}) : page_body(BoolC<true>{})) {
               failed = true;
               g_fail = g - 1;
             }
