@@ -1562,63 +1562,76 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
 // One work unit = (sequence, head block, 64-channel chunk); a thread owns one
 // head and 8 channels, so all partials of a unit are read in one batch.
 constexpr int kCombineBatch = 16;
+constexpr int kCombineChunks = 16;  // 32-channel chunks of a head block
 __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
-  pdl_wait();
   const int tid = threadIdx.x;
-  const int hc = tid >> 3, c8 = (tid & 7) * 8;
-  const int units = p.B * p.HB * 8;
-  for (int u = blockIdx.x; u < units; u += gridDim.x) {
-    const int chunk = u & 7, rest = u >> 3;
+  const int hc = tid >> 3, c4 = (tid & 7) * 4;  // head in the block, 4 channels of the chunk
+  const int units = p.B * p.HB * kCombineChunks;
+  // The item ranges come from the plan, which completed before the decode
+  // grid started (and so before this grid was launched): they are read
+  // before waiting for the decode grid.
+  int u = blockIdx.x;
+  int s0 = 0, s1 = 0;
+  if (u < units) {
+    const int b = (u / kCombineChunks) / p.HB;
+    s0 = p.item_start[b];
+    s1 = p.item_start[b + 1];
+  }
+  pdl_wait();
+  for (; u < units; u += gridDim.x) {
+    const int chunk = u % kCombineChunks, rest = u / kCombineChunks;
     const int hb = rest % p.HB, b = rest / p.HB;
-    const int s0 = p.item_start[b], s1 = p.item_start[b + 1];
+    if (u != (int)blockIdx.x) {
+      s0 = p.item_start[b];
+      s1 = p.item_start[b + 1];
+    }
     if (s1 - s0 < 2) continue;  // finalized by the decode kernel
     const int row = 16 * hb + hc;
-    const int c = 64 * chunk + c8;
-    float m = -INFINITY;
+    const int c = (kDL / kCombineChunks) * chunk + c4;
+    // one pass over the partials, kCombineBatch at a time, with a running max
+    float m = -INFINITY, tot = 0.f;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int k0 = s0; k0 < s1; k0 += kCombineBatch) {
+      uint2 v[kCombineBatch];
       float l[kCombineBatch];
 #pragma unroll
-      for (int k = 0; k < kCombineBatch; ++k)
-        l[k] = k0 + k < s1 ? __ldcg(&p.lse_part[(size_t)(k0 + k) * p.H + row]) : -INFINITY;
+      for (int k = 0; k < kCombineBatch; ++k) {
+        const bool in = k0 + k < s1;
+        l[k] = in ? __ldcg(&p.lse_part[(size_t)(k0 + k) * p.H + row]) : -INFINITY;
+        v[k] = in ? __ldcg(reinterpret_cast<const uint2*>(p.o_part + ((size_t)(k0 + k) * p.H + row) * kDL + c))
+                  : make_uint2(0u, 0u);
+      }
+      float mb = m;
 #pragma unroll
-      for (int k = 0; k < kCombineBatch; ++k) m = fmaxf(m, l[k]);
-    }
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float tot = 0.f;
-    if (m != -INFINITY) {
-      for (int k0 = s0; k0 < s1; k0 += kCombineBatch) {
-        uint4 v[kCombineBatch];
-        float l[kCombineBatch];
+      for (int k = 0; k < kCombineBatch; ++k) mb = fmaxf(mb, l[k]);
+      if (mb == -INFINITY) continue;  // no tokens so far
+      const float sc = expf(m - mb);  // 0 while m = -inf
+      tot *= sc;
 #pragma unroll
-        for (int k = 0; k < kCombineBatch; ++k) {
-          const bool in = k0 + k < s1;
-          l[k] = in ? __ldcg(&p.lse_part[(size_t)(k0 + k) * p.H + row]) : -INFINITY;
-          v[k] = in ? __ldcg(reinterpret_cast<const uint4*>(p.o_part + ((size_t)(k0 + k) * p.H + row) * kDL + c))
-                    : make_uint4(0u, 0u, 0u, 0u);
-        }
+      for (int e = 0; e < 4; ++e) acc[e] *= sc;
 #pragma unroll
-        for (int k = 0; k < kCombineBatch; ++k) {
-          const float wgt = expf(l[k] - m);  // 0 for padding (lse = -inf)
-          tot += wgt;
-          const __half2* hv = reinterpret_cast<const __half2*>(&v[k]);
+      for (int k = 0; k < kCombineBatch; ++k) {
+        const float wgt = expf(l[k] - mb);  // 0 for padding (lse = -inf)
+        tot += wgt;
+        const __half2* hv = reinterpret_cast<const __half2*>(&v[k]);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __half22float2(hv[e]);
-            acc[2 * e] = fmaf(wgt, f.x, acc[2 * e]);
-            acc[2 * e + 1] = fmaf(wgt, f.y, acc[2 * e + 1]);
-          }
+        for (int e = 0; e < 2; ++e) {
+          const float2 f = __half22float2(hv[e]);
+          acc[2 * e] = fmaf(wgt, f.x, acc[2 * e]);
+          acc[2 * e + 1] = fmaf(wgt, f.y, acc[2 * e + 1]);
         }
       }
+      m = mb;
     }
     const float inv = tot > 0.f ? 1.f / tot : 0.f;
-    uint4 pk;
+    uint2 pk;
     uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
+    for (int e = 0; e < 2; ++e) {
       const __nv_bfloat162 bv = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
       pw[e] = *reinterpret_cast<const uint32_t*>(&bv);
     }
-    *reinterpret_cast<uint4*>(p.out + ((size_t)b * p.H + row) * kDL + c) = pk;
+    *reinterpret_cast<uint2*>(p.out + ((size_t)b * p.H + row) * kDL + c) = pk;
     if (chunk == 0 && (tid & 7) == 0) p.lse[(size_t)b * p.H + row] = tot > 0.f ? m + logf(tot) : -INFINITY;
   }
 }
@@ -1661,7 +1674,7 @@ static cudaError_t run_decode(mlaq_cache* c, const DecodeParams& p, int grid_cta
     ev = reinterpret_cast<cudaEvent_t*>(c->timing_events) + 2 * c->timing_n;  // ev[0] precedes the plan
   cudaError_t e = launch_pdl(decode_kernel<MODE>, dim3(p.HB, grid_cta), dim3(kThreads), smem, s, p);
   if (e == cudaSuccess) {
-    const int units = p.B * p.HB * 8;
+    const int units = p.B * p.HB * kCombineChunks;
     e = launch_pdl(combine_kernel, dim3(max(1, min(units, 2 * c->decode_ctas))), dim3(128), 0, s, p);
   }
   if (ev) {
