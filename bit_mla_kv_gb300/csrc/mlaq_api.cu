@@ -12,6 +12,22 @@ int launch_decode_static(int mode, const void* codes, const void* meta, const vo
                          uint16_t* out, float* lse, int32_t* dev_status, cudaStream_t s);
 }
 
+namespace mlaq {
+// One warp waits on an mbarrier that nothing (arrive = 0) or its own thread 0
+// (arrive = 1) completes, through the bounded wait of the decode kernel.
+__global__ void wait_probe_kernel(int32_t* status, uint64_t limit_ns, int arrive) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (arrive) mbar_arrive_expect_tx(&bar, 0);
+  }
+  __syncthreads();
+  const bool ok = mbar_wait_bounded(&bar, 0, limit_ns);
+  if (threadIdx.x == 0) *status = ok ? 0 : MLAQ_DEV_TIMEOUT;
+}
+}  // namespace mlaq
+
 using namespace mlaq;
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -235,6 +251,13 @@ int mlaq_set_decode_ctas(mlaq_cache* c, int32_t ctas) {
   if (ctas <= 0 || ctas > kMaxPlanCtas) return MLAQ_ERR_SHAPE;
   c->decode_ctas = ctas;
   return MLAQ_OK;
+}
+
+int mlaq_debug_wait_probe(int32_t* status, int32_t wait_us, int32_t arrive, struct CUstream_st* stream) {
+  if (!status) return MLAQ_ERR_NULL;
+  if (wait_us < 1 || wait_us > 100000 || (arrive != 0 && arrive != 1)) return MLAQ_ERR_SHAPE;
+  wait_probe_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(status, (uint64_t)wait_us * 1000u, arrive);
+  return cudaGetLastError() == cudaSuccess ? MLAQ_OK : MLAQ_ERR_CUDA;
 }
 
 }  // extern "C"

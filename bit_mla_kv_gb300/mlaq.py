@@ -34,7 +34,7 @@ EXPORTED = [
     "mlaq_buffer_sizes", "mlaq_cache_create", "mlaq_cache_destroy", "mlaq_append", "mlaq_decode",
     "mlaq_export_tokens", "mlaq_cache_bytes", "mlaq_get_device_status", "mlaq_clear_device_status",
     "mlaq_timing_enable", "mlaq_timing_read", "mlaq_set_decode_ctas", "mlaq_status_string",
-    "mlaq_decode_noalloc",
+    "mlaq_decode_noalloc", "mlaq_debug_wait_probe",
 ]
 
 _lib.mlaq_status_string.restype = ctypes.c_char_p
@@ -54,6 +54,7 @@ _lib.mlaq_timing_read.argtypes = [_vp, ctypes.POINTER(ctypes.c_float), ctypes.PO
 _lib.mlaq_set_decode_ctas.argtypes = [_vp, _i32]
 _lib.mlaq_decode_noalloc.argtypes = [ctypes.c_int, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _i32,
                                      ctypes.c_float, _vp, _vp, _vp, _vp]
+_lib.mlaq_debug_wait_probe.argtypes = [_vp, _i32, _i32, _vp]
 for _name in EXPORTED:
     if _name != "mlaq_status_string":
         getattr(_lib, _name).restype = ctypes.c_int
@@ -97,6 +98,14 @@ def buffer_sizes(mode: str, num_pages: int, max_seqs: int, max_heads: int):
     _check(_lib.mlaq_buffer_sizes(MODES[mode], num_pages, max_seqs, max_heads, *[ctypes.byref(o) for o in out]),
            "mlaq_buffer_sizes")
     return tuple(o.value for o in out)
+
+
+def debug_wait_probe(status, wait_us: int, arrive: bool, stream=None):
+    """Runs the bounded-wait test hook into `status` (int32 CUDA tensor of one
+    element): MLAQ_DEV_TIMEOUT when the wait ran out, 0 when it completed."""
+    _need(status, torch.int32, (1,), "status")
+    _check(_lib.mlaq_debug_wait_probe(_ptr(status), int(wait_us), 1 if arrive else 0, _stream(stream)),
+           "mlaq_debug_wait_probe")
 
 
 def _bf16_rows_in_channel_order(raw):

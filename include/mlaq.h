@@ -223,6 +223,18 @@ int mlaq_timing_read(mlaq_cache* cache, float* ms_out, int32_t* n);
 /* Number of CTAs the decode planner aims to fill (default 2 per SM). */
 int mlaq_set_decode_ctas(mlaq_cache* cache, int32_t ctas);
 
+/* Test hook for the bounded waits behind MLAQ_DEV_TIMEOUT (the decode kernel
+ * waits on mbarriers for its bulk copies and its tensor-core MMAs, each wait
+ * limited in wall time, never a trap). Launches one CTA of 32 threads that
+ * waits on a shared-memory mbarrier through that same bounded wait with a
+ * limit of wait_us microseconds. arrive = 0: nothing completes the barrier,
+ * the wait runs out and the kernel stores MLAQ_DEV_TIMEOUT in *status;
+ * arrive = 1: the CTA completes the barrier first and stores 0. status is a
+ * device pointer to one int32 owned by the caller. Asynchronous on `stream`.
+ * Returns MLAQ_ERR_NULL for a NULL status, MLAQ_ERR_SHAPE for wait_us outside
+ * [1, 100000] or arrive outside {0, 1}, MLAQ_ERR_CUDA if the launch fails. */
+int mlaq_debug_wait_probe(int32_t* status, int32_t wait_us, int32_t arrive, struct CUstream_st* stream);
+
 const char* mlaq_status_string(int status);
 
 #ifdef __cplusplus

@@ -178,6 +178,30 @@ def test_device_status_reports_bad_page_without_fault():
     assert case.cache.device_status() == 0
 
 
+def test_bounded_wait_runs_out_and_reports_status():
+    # A wait on an mbarrier that nothing completes ends after its limit with
+    # the timeout status (no trap, no hang), and the context stays usable.
+    import time
+    from bit_mla_kv_gb300.mlaq import DEV_TIMEOUT, debug_wait_probe
+    st = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    debug_wait_probe(st, 5000, arrive=False)
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    assert int(st.item()) == DEV_TIMEOUT
+    assert waited >= 0.004  # the 5 ms limit, measured on the device timer
+    st.fill_(-1)
+    debug_wait_probe(st, 5000, arrive=True)
+    assert int(st.item()) == 0
+    case = Case("C4R4", [700], 16, seed=3)
+    case.build()
+    out, lse = case.decode()
+    ro, rl = case.oracle_seq(0)
+    assert_close_out(out[0], lse[0], ro, rl, "decode after a timed-out wait")
+    assert case.cache.device_status() == 0
+
+
 @pytest.mark.parametrize("name,sample", [("v2lite_c4r4", [0, 7, 19, 31]), ("v3_c4r4", [0, 63]),
                                          ("long_c2r4", [2]), ("long_c4r4", [1]), ("long_bf16", [3])])
 def test_full_size_sampled(name, sample):
