@@ -45,26 +45,18 @@ constexpr int kStages = MLAQ_STAGES;
 constexpr int kT = 16;                                // tokens per step
 constexpr int kRingChunks = (kRing + kT - 1) / kT;    // 9
 constexpr int kStageBytes = kPage * 288 + kMetaPage;  // 20736: max(C4R4 page + meta, 16 BF16 tokens)
-constexpr int kPStride = 40;   // halfs per row of P [h][t] (32 tokens; 80-byte rows for ldmatrix)
 constexpr uint64_t kWaitLimit = 200000000ull;  // 200 ms per bounded wait
 constexpr int kMaxDevices = 64;
 template <bool B>
 struct BoolC {
   static constexpr bool value = B;
 };
-// MLAQ_TC_AGG=1 (default): aggregation on tcgen05 with O^T in TMEM, whole
-// valid pages as one step. MLAQ_TC_AGG=0: register MMAs, half-page steps.
-#ifndef MLAQ_TC_AGG
-#define MLAQ_TC_AGG 1
-#endif
-// floats per row of partial scores [h][t]: 32 tokens (52 = 20 mod 32), or 64 with tcgen05 page steps
-constexpr int kSpStride = MLAQ_TC_AGG ? 68 : 52;
-#if MLAQ_TC_AGG
-// Aggregation on tcgen05 (MLAQ_TC_AGG): O^T[channel][head] accumulates in TMEM.
+// floats per row of partial scores [h][t]: 64 tokens of a page step + 4 (bank spread)
+constexpr int kSpStride = 68;
+// Aggregation on tcgen05: O^T[channel][head] accumulates in TMEM.
 constexpr int kAggBufs = 2;      // A (content) / P^T step buffers in flight
 constexpr int kTmemCols = 256;   // O^T: 4 blocks x 16 heads; A: 4 sub-steps x 4 blocks x 8 columns
 constexpr int kTmemA = 64;       // first column of the A step buffers
-#endif
 
 struct DecodeParams {
   const uint8_t* codes;
@@ -87,22 +79,19 @@ struct DecodeParams {
   float scale_log2;
 };
 
-struct __align__(16) DecodeSmem {
+struct __align__(128) DecodeSmem {
   uint8_t stage[kStages][kStageBytes];
   float sp[kWarps][16][kSpStride];  // partial scores, [warp][head][token]
-  __half pr[16][kPStride];          // P, [head][token]
   float alpha[16];
   float fin_m[16];
   float fin_l[16];
   int stage_bad[kStages];
   uint64_t full[kStages];
-#if MLAQ_TC_AGG
   __align__(128) uint8_t pt[kAggBufs][512];  // P^T B operand: 16 heads x 16 tokens, 8x8 core matrices
   __align__(128) uint8_t ptp[4][512];        // P^T of the four sub-steps of a page step
   uint64_t agg_done[kAggBufs];
   uint32_t tmem_base;
   int rescale_flag[kWarps];
-#endif
 };
 
 __device__ __forceinline__ int clamp_len(int L, int max_tokens) { return min(max(L, 0), max_tokens); }
@@ -509,27 +498,21 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(&sm.full[s], 1);
-#if MLAQ_TC_AGG
     for (int s = 0; s < kAggBufs; ++s) mbar_init(&sm.agg_done[s], kWarps);
-#endif
     fence_mbar_init();
     fence_proxy_async();
   }
-#if MLAQ_TC_AGG
   if (w == 0) {
     tmem_alloc(&sm.tmem_base, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
-#endif
   __syncthreads();
-#if MLAQ_TC_AGG
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   int agg_ctr = 0;    // aggregation steps issued by this CTA
   int page_ctr = -1;  // the last of them that was a page step (reads every A column)
   constexpr uint32_t kAggIdesc = umma_idesc_f16(128, 16);
-#endif
   ProdCursor pc;
   if (tid == 0) {
     producer_init<MODE>(p, pc, first, i0, i1);
@@ -597,19 +580,7 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
       }
     }
 
-#if MLAQ_TC_AGG
     bool item_first = true;  // the item's first aggregation MMA overwrites O^T
-#else
-    float o[2][4][2][4];  // O[h = r / r+8][c = 64(2w+j) + 16kk + 8cb + 2i..]
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-        for (int cb = 0; cb < 2; ++cb)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) o[j][kk][cb][e] = 0.f;
-#endif
     float m_run = -INFINITY, l_run = 0.f;
 
     const int nst = item_stages<MODE>(it, L);
@@ -793,7 +764,6 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
             ch[j][kk][3] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][3]), s2y, m2y)));
           }
         }
-#if MLAQ_TC_AGG
         // content tile -> TMEM A step buffer (lanes = channels, columns = token pairs)
         const int ab = agg_ctr % kAggBufs;
         bool agg_ok = true;
@@ -815,9 +785,6 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
           }
         tmem_wait_st();
         tc_fence_before();
-#else
-        const bool agg_ok = true;
-#endif
         // barrier 1: partial scores complete; also agrees on a timed-out wait
         if (named_bar_or(1, kThreads, !(ok && agg_ok))) return true;
         // the stage's shared memory is no longer read: refill it with the
@@ -852,7 +819,6 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
           const float mref = (m_run == -INFINITY) ? 0.f : m_run;  // nothing valid yet: x = -inf -> p = 0
           const float p0 = ex2(x0 - mref), p1 = ex2(x1 - mref);
           l_run = l_run * alpha + (p0 + p1);
-#if MLAQ_TC_AGG
           {
             // P^T[head hh][k] with token k order matching the TMEM A columns
             const int kp = tp < 8 ? 2 * tp : 2 * tp - 14;
@@ -862,14 +828,10 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
             const bool any_rs = __any_sync(0xffffffffu, alpha != 1.f);
             if (lane == 0) sm.rescale_flag[w] = any_rs;
           }
-#else
-          *reinterpret_cast<__half2*>(&sm.pr[hh][tp]) = __floats2half2_rn(p0, p1);
-#endif
           if ((lane & 7) == 0) sm.alpha[hh] = alpha;
         }
         named_bar_sync(2, kThreads);
         // ---------------- aggregation
-#if MLAQ_TC_AGG
         {
           const bool need_rs = !item_first && (sm.rescale_flag[0] | sm.rescale_flag[1] | sm.rescale_flag[2] |
                                                sm.rescale_flag[3]);
@@ -906,237 +868,11 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
           item_first = false;
           agg_ctr++;
         }
-#else
-        // ---------------- aggregation
-        {
-          const float ar = sm.alpha[r], ar8 = sm.alpha[r + 8];
-          if (__any_sync(0xffffffffu, ar != 1.f || ar8 != 1.f)) {
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-                for (int cb = 0; cb < 2; ++cb) {
-                  o[j][kk][cb][0] *= ar;
-                  o[j][kk][cb][1] *= ar;
-                  o[j][kk][cb][2] *= ar8;
-                  o[j][kk][cb][3] *= ar8;
-                }
-          }
-          uint32_t pa[4];
-          ldmatrix_x4(pa, &sm.pr[(lane & 7) + 8 * ((lane >> 3) & 1)][8 * (lane >> 4)]);
-#pragma unroll
-          for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              // channel block cb = 0: B = (movmatrix of a0, a1); cb = 1: (a2, a3)
-              mma16816(o[j][kk][0], pa, ch[j][kk][0], ch[j][kk][1]);
-              mma16816(o[j][kk][1], pa, ch[j][kk][2], ch[j][kk][3]);
-            }
-        }
-#endif
         // No barrier before the next step's writes to sp: every thread passed
         // barrier 2 after all reads of sp; pr/alpha are rewritten only after
         // the next barrier 1, which all threads reach after their reads.
         return false;
       };
-#if !MLAQ_TC_AGG
-      // Half a packed page (32 tokens, all valid) as two 16-token sub-steps
-      // under one pair of barriers: half the synchronisation per token of
-      // the 16-token step. The dequantized, transposed content fragments of
-      // both sub-steps stay in registers until the aggregation.
-      auto half_body = [&](const int s2) -> bool {
-        uint32_t vt[2][2][4][4];
-        const uint8_t* mtab = st + page_code_bytes(MODE);
-#pragma unroll
-        for (int sub = 0; sub < 2; ++sub) {
-          const int lr = 32 * s2 + 16 * sub + r;
-          uint32_t mx[3], my[3];
-#pragma unroll
-          for (int j = 0; j < 3; ++j) {
-            const int gg = j < 2 ? 2 * w + j : 8;
-            mx[j] = *reinterpret_cast<const uint32_t*>(mtab + lr * kMetaTok + 4 * gg);
-            my[j] = *reinterpret_cast<const uint32_t*>(mtab + (lr + 8) * kMetaTok + 4 * gg);
-          }
-          uint32_t (&ch)[2][4][4] = vt[sub];
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int gg = 2 * w + j;
-            if constexpr (CBITS == 4) {
-              const uint2 wx = *reinterpret_cast<const uint2*>(st + lr * CB + gg * GBYTES + 8 * i);
-              const uint2 wy = *reinterpret_cast<const uint2*>(st + (lr + 8) * CB + gg * GBYTES + 8 * i);
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t ax = (kk >> 1) ? wx.y : wx.x, ay = (kk >> 1) ? wy.y : wy.x;
-                const uint32_t ax8 = ax >> 8, ay8 = ay >> 8;
-                const int p0 = 2 * (kk & 1);
-                ch[j][kk][0] = int4_pos(ax, ax8, p0);
-                ch[j][kk][1] = int4_pos(ay, ay8, p0);
-                ch[j][kk][2] = int4_pos(ax, ax8, p0 + 1);
-                ch[j][kk][3] = int4_pos(ay, ay8, p0 + 1);
-              }
-            } else {
-              const uint32_t ax = *reinterpret_cast<const uint32_t*>(st + lr * CB + gg * GBYTES + 4 * i);
-              const uint32_t ay = *reinterpret_cast<const uint32_t*>(st + (lr + 8) * CB + gg * GBYTES + 4 * i);
-              const uint32_t ax8 = ax >> 8, ay8 = ay >> 8;
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                ch[j][kk][0] = int2_pos(ax, ax8, 2 * kk);
-                ch[j][kk][1] = int2_pos(ay, ay8, 2 * kk);
-                ch[j][kk][2] = int2_pos(ax, ax8, 2 * kk + 1);
-                ch[j][kk][3] = int2_pos(ay, ay8, 2 * kk + 1);
-              }
-            }
-          }
-          uint32_t rf[4];
-          {
-            uint32_t ax = *reinterpret_cast<const uint32_t*>(st + lr * CB + ROPE_OFF + 4 * (2 * w + (i >> 1)));
-            uint32_t ay = *reinterpret_cast<const uint32_t*>(st + (lr + 8) * CB + ROPE_OFF + 4 * (2 * w + (i >> 1)));
-            if (i & 1) {
-              ax >>= 8;
-              ay >>= 8;
-            }
-            rf[0] = int4_pos(ax, 0u, 0);
-            rf[1] = int4_pos(ay, 0u, 0);
-            rf[2] = int4_pos(ax, 0u, 1);
-            rf[3] = int4_pos(ay, 0u, 1);
-          }
-          float sacc[2][4];
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sacc[hb][e] = 0.f;
-          {
-            uint32_t a[4];
-            const uint32_t mnx = (i == 0) ? mx[0] : (i == 1) ? mx[1] : mx[2];
-            const uint32_t mny = (i == 0) ? my[0] : (i == 1) ? my[1] : my[2];
-            a[0] = (i < 3) ? __byte_perm(mnx, 0, 0x3232) : 0u;
-            a[1] = (i < 3) ? __byte_perm(mny, 0, 0x3232) : 0u;
-            a[2] = 0u;
-            a[3] = 0u;
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb) mma16816(sacc[hb], a, kmn[hb], 0u);
-          }
-          {
-            float d0[2][4], d1[2][4], d2[2][4];
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) d0[hb][e] = d1[hb][e] = d2[hb][e] = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              mma16816(d0[0], ch[0][kk], qf[0][kk][0][0], qf[0][kk][0][1]);
-              mma16816(d1[0], ch[1][kk], qf[1][kk][0][0], qf[1][kk][0][1]);
-              mma16816(d0[1], ch[0][kk], qf[0][kk][1][0], qf[0][kk][1][1]);
-              mma16816(d1[1], ch[1][kk], qf[1][kk][1][0], qf[1][kk][1][1]);
-            }
-            mma16816(d2[0], rf, qr[0][0], qr[0][1]);
-            mma16816(d2[1], rf, qr[1][0], qr[1][1]);
-            float sxv[3], syv[3];
-#pragma unroll
-            for (int j = 0; j < 3; ++j) {
-              sxv[j] = __half2float(__ushort_as_half((unsigned short)(mx[j] & 0xffffu)));
-              syv[j] = __half2float(__ushort_as_half((unsigned short)(my[j] & 0xffffu)));
-            }
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {
-              sacc[hb][0] = fmaf(sxv[2], d2[hb][0], fmaf(sxv[1], d1[hb][0], fmaf(sxv[0], d0[hb][0], sacc[hb][0])));
-              sacc[hb][1] = fmaf(sxv[2], d2[hb][1], fmaf(sxv[1], d1[hb][1], fmaf(sxv[0], d0[hb][1], sacc[hb][1])));
-              sacc[hb][2] = fmaf(syv[2], d2[hb][2], fmaf(syv[1], d1[hb][2], fmaf(syv[0], d0[hb][2], sacc[hb][2])));
-              sacc[hb][3] = fmaf(syv[2], d2[hb][3], fmaf(syv[1], d1[hb][3], fmaf(syv[0], d0[hb][3], sacc[hb][3])));
-            }
-          }
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb) {
-            const int h = 8 * hb + 2 * i;
-            const int t = 16 * sub + r;
-            sm.sp[w][h][t] = sacc[hb][0];
-            sm.sp[w][h + 1][t] = sacc[hb][1];
-            sm.sp[w][h][t + 8] = sacc[hb][2];
-            sm.sp[w][h + 1][t + 8] = sacc[hb][3];
-          }
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const __half2 s2x = __low2half2(u32_as_h2(mx[j])), m2x = __high2half2(u32_as_h2(mx[j]));
-            const __half2 s2y = __low2half2(u32_as_h2(my[j])), m2y = __high2half2(u32_as_h2(my[j]));
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              ch[j][kk][0] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][0]), s2x, m2x)));
-              ch[j][kk][1] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][1]), s2y, m2y)));
-              ch[j][kk][2] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][2]), s2x, m2x)));
-              ch[j][kk][3] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][3]), s2y, m2y)));
-            }
-          }
-        }
-        // barrier 1: partial scores of 32 tokens complete; agrees on a timed-out wait
-        if (named_bar_or(1, kThreads, !ok)) return true;
-        if (tid == 0 && s2 == 1) producer_advance<MODE>(p, sm, pc, i1);
-        // online softmax for head hh, tokens tq .. tq + 3
-        {
-          const int tq = 4 * (lane & 7);
-          float x[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int ww = 0; ww < kWarps; ++ww) {
-            const float4 v = *reinterpret_cast<const float4*>(&sm.sp[ww][hh][tq]);
-            x[0] += v.x;
-            x[1] += v.y;
-            x[2] += v.z;
-            x[3] += v.w;
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) x[u] *= p.scale_log2;
-          const float xm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-          float alpha = 1.f;
-          if (__any_sync(0xffffffffu, xm > m_run + 8.f)) {
-            float tmax = xm;
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
-            const bool upd = tmax > m_run + 8.f;
-            alpha = upd ? ex2(m_run - tmax) : 1.f;
-            m_run = upd ? tmax : m_run;
-          }
-          const float p0 = ex2(x[0] - m_run), p1 = ex2(x[1] - m_run);
-          const float p2 = ex2(x[2] - m_run), p3 = ex2(x[3] - m_run);
-          l_run = l_run * alpha + ((p0 + p1) + (p2 + p3));
-          const __half2 q01 = __floats2half2_rn(p0, p1), q23 = __floats2half2_rn(p2, p3);
-          *reinterpret_cast<uint2*>(&sm.pr[hh][tq]) = make_uint2(h2_as_u32(q01), h2_as_u32(q23));
-          if ((lane & 7) == 0) sm.alpha[hh] = alpha;
-        }
-        named_bar_sync(2, kThreads);
-        // aggregation over both sub-steps
-        {
-          const float ar = sm.alpha[r], ar8 = sm.alpha[r + 8];
-          if (__any_sync(0xffffffffu, ar != 1.f || ar8 != 1.f)) {
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-                for (int cb = 0; cb < 2; ++cb) {
-                  o[j][kk][cb][0] *= ar;
-                  o[j][kk][cb][1] *= ar;
-                  o[j][kk][cb][2] *= ar8;
-                  o[j][kk][cb][3] *= ar8;
-                }
-          }
-          uint32_t pa[2][4];
-          ldmatrix_x4(pa[0], &sm.pr[(lane & 7) + 8 * ((lane >> 3) & 1)][8 * (lane >> 4)]);
-          ldmatrix_x4(pa[1], &sm.pr[(lane & 7) + 8 * ((lane >> 3) & 1)][16 + 8 * (lane >> 4)]);
-#pragma unroll
-          for (int sub = 0; sub < 2; ++sub)
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                mma16816(o[j][kk][0], pa[sub], vt[sub][j][kk][0], vt[sub][j][kk][1]);
-                mma16816(o[j][kk][1], pa[sub], vt[sub][j][kk][2], vt[sub][j][kk][3]);
-              }
-        }
-        return false;
-      };
-#endif
-#if MLAQ_TC_AGG
       // A whole packed page (64 tokens, all valid) under one pair of
       // barriers. The four 16-token sub-steps store their dequantized,
       // transposed content tiles in TMEM (A operand, lanes = channels) and
@@ -1393,35 +1129,6 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
         }
         return false;
       };
-#endif
-#if !MLAQ_TC_AGG
-      if constexpr (MODE != MLAQ_BF16) {
-        // packed stage: all-valid halves take the 32-token body; the decision
-        // uses only CTA-uniform values (a timed-out wait is caught at barrier 1)
-        if (packed) {
-          bool fail = false;
-          for (int s2 = 0; s2 < 2 && !fail; ++s2) {
-            const int t0 = kPage * sref.idx + 32 * s2;
-            if (!bad && t0 >= kSink && t0 + 32 <= L - kRecent) {
-              fail = half_body(s2);
-            } else {
-              for (int q = 0; q < 2 && !fail; ++q) {
-                const int s = 2 * s2 + q;
-                const int t1 = t0 + kT * q;
-                const bool full = ok & !bad & (t1 >= kSink) & (t1 + kT <= L - kRecent);
-                fail = full ? step_body(BoolC<true>{}, s) : step_body(BoolC<false>{}, s);
-              }
-            }
-          }
-          if (fail) {
-            failed = true;
-            g_fail = g - 1;
-          }
-          continue;
-        }
-      }
-#endif
-#if MLAQ_TC_AGG
       if constexpr (MODE != MLAQ_BF16) {
         if (packed) {
           const int t0 = kPage * sref.idx;
@@ -1435,7 +1142,6 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
           }
         }
       }
-#endif
       for (int s = 0; s < nsteps; ++s) {
         bool full = false;
         if (packed) {
@@ -1470,7 +1176,6 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
     // A sequence with a single item is final here (bf16 out, lse); otherwise
     // the normalized partial (fp16) and its lse go to the combine kernel.
     __half* op = p.o_part + ((size_t)item_idx * H + h0) * kDL;
-#if MLAQ_TC_AGG
     {
       // O^T lane l of block blk holds channel 128 (l/32) + 64 (blk/2) + 16 (2 (blk%2) + (l%32)/16) + l%16
       if (agg_ctr > 0) {
@@ -1502,32 +1207,6 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
       }
       tc_fence_before();
     }
-#else
-    {
-      const float lr0 = sm.fin_l[r], lr8 = sm.fin_l[r + 8];
-      const float inv0 = lr0 > 0.f ? 1.f / lr0 : 0.f, inv8 = lr8 > 0.f ? 1.f / lr8 : 0.f;
-      uint16_t* fo = p.out + ((size_t)it.b * H + h0) * kDL;
-#pragma unroll
-      for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-          for (int cb = 0; cb < 2; ++cb) {
-            const int c = 64 * (2 * w + j) + 16 * kk + 8 * cb + 2 * i;
-            if (single) {
-              const __nv_bfloat162 v0 = __floats2bfloat162_rn(o[j][kk][cb][0] * inv0, o[j][kk][cb][1] * inv0);
-              const __nv_bfloat162 v1 = __floats2bfloat162_rn(o[j][kk][cb][2] * inv8, o[j][kk][cb][3] * inv8);
-              *reinterpret_cast<__nv_bfloat162*>(fo + (size_t)r * kDL + c) = v0;
-              *reinterpret_cast<__nv_bfloat162*>(fo + (size_t)(r + 8) * kDL + c) = v1;
-            } else {
-              *reinterpret_cast<__half2*>(op + (size_t)r * kDL + c) =
-                  __floats2half2_rn(o[j][kk][cb][0] * inv0, o[j][kk][cb][1] * inv0);
-              *reinterpret_cast<__half2*>(op + (size_t)(r + 8) * kDL + c) =
-                  __floats2half2_rn(o[j][kk][cb][2] * inv8, o[j][kk][cb][3] * inv8);
-            }
-          }
-    }
-#endif
     if (tid < 16) {
       const float l = sm.fin_l[tid];
       const float lse_v = l > 0.f ? (sm.fin_m[tid] + log2f(l)) * 0.69314718055994531f : -INFINITY;
@@ -1545,13 +1224,11 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
     for (int gg = g_fail; gg < pc.issued; ++gg)
       mbar_wait_bounded(&sm.full[gg % kStages], (gg / kStages) & 1, kWaitLimit);
   }
-#if MLAQ_TC_AGG
   // every aggregation MMA has completed (waited for in each item epilogue)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (w == 0) tmem_dealloc(tmem, kTmemCols);
-#endif
 }
 
 // ---------------------------------------------------------------------------
