@@ -55,8 +55,10 @@ struct BoolC {
 constexpr int kSpStride = 68;
 // Aggregation on tcgen05: O^T[channel][head] accumulates in TMEM.
 constexpr int kAggBufs = 2;      // A (content) / P^T step buffers in flight
-constexpr int kTmemCols = 256;   // O^T: 4 blocks x 16 heads; A: 4 sub-steps x 4 blocks x 8 columns
-constexpr int kTmemA = 64;       // first column of the A step buffers
+constexpr int kTmemCols = 256;   // O^T: 4 blocks x NH heads, then A: 4 sub-steps x 4 blocks x 8 columns
+// first TMEM column of the A step buffers for NH heads per CTA
+template <int NH>
+__host__ __device__ constexpr uint32_t tmem_a_col() { return 4 * NH; }
 
 struct DecodeParams {
   const uint8_t* codes;
@@ -79,20 +81,31 @@ struct DecodeParams {
   float scale_log2;
 };
 
+// Shared memory of a decode CTA serving NH heads (16, or 32 when H is a
+// multiple of 32: the two 16-head halves then share every page's unpack; the
+// larger score and P tiles and the second half's query fragments leave room
+// for two stages at two CTAs per SM).
+template <int NH>
 struct __align__(128) DecodeSmem {
-  uint8_t stage[kStages][kStageBytes];
-  float sp[kWarps][16][kSpStride];  // partial scores, [warp][head][token]
-  float alpha[16];
-  float fin_m[16];
-  float fin_l[16];
-  int stage_bad[kStages];
-  uint64_t full[kStages];
-  __align__(128) uint8_t pt[kAggBufs][512];  // P^T B operand: 16 heads x 16 tokens, 8x8 core matrices
-  __align__(128) uint8_t ptp[4][512];        // P^T of the four sub-steps of a page step
+  static constexpr int kNumStages = NH == 16 ? kStages : 2;
+  static constexpr int kQxWords = NH == 16 ? 1 : 10 * kThreads;  // 38 fragment words per thread, as uint4
+  uint8_t stage[kNumStages][kStageBytes];
+  float sp[kWarps][NH][kSpStride];  // partial scores, [warp][head][token]
+  float alpha[NH];
+  float fin_m[NH];
+  float fin_l[NH];
+  int stage_bad[kNumStages];
+  uint64_t full[kNumStages];
+  __align__(128) uint8_t pt[kAggBufs][32 * NH];  // P^T B operand: NH heads x 16 tokens, 8x8 core matrices
+  __align__(128) uint8_t ptp[4][32 * NH];        // P^T of the four sub-steps of a page step
   uint64_t agg_done[kAggBufs];
   uint32_t tmem_base;
   int rescale_flag[kWarps];
+  uint4 qx[kQxWords];  // query fragments of heads 16..31 of the block, [word / 4][thread]
 };
+// two CTAs per SM: 228 KB of shared memory, 1 KB of it reserved per CTA
+static_assert(sizeof(DecodeSmem<16>) <= 113 * 1024 && sizeof(DecodeSmem<32>) <= 113 * 1024,
+              "decode shared memory must allow two CTAs per SM");
 
 __device__ __forceinline__ int clamp_len(int L, int max_tokens) { return min(max(L, 0), max_tokens); }
 // Units of a sequence and its leading ring units.
@@ -400,8 +413,8 @@ __device__ __forceinline__ bool row_valid(const StageRef& st, int j, int L) {
 }
 
 // Producer: issue the bulk copies of a stage into buffer `buf`.
-template <int MODE>
-__device__ void issue_stage(const DecodeParams& p, DecodeSmem& sm, int b, const StageRef& st, int page, int buf) {
+template <int MODE, class SM>
+__device__ void issue_stage(const DecodeParams& p, SM& sm, int b, const StageRef& st, int page, int buf) {
   uint64_t* bar = &sm.full[buf];
   if (st.kind == 0) {
     const int base = kT * st.idx;
@@ -459,10 +472,10 @@ __device__ void producer_init(const DecodeParams& p, ProdCursor& pc, const Item&
   if (i0 + 1 < i1) pc.nxt = p.items[i0 + 1];
   pc.page = first.pad0;
 }
-template <int MODE>
-__device__ void producer_advance(const DecodeParams& p, DecodeSmem& sm, ProdCursor& pc, int i1) {
+template <int MODE, class SM>
+__device__ void producer_advance(const DecodeParams& p, SM& sm, ProdCursor& pc, int i1) {
   if (pc.item >= i1) return;
-  issue_stage<MODE>(p, sm, pc.cur.b, item_stage<MODE>(pc.cur, pc.cur.L, pc.k), pc.page, pc.issued % kStages);
+  issue_stage<MODE>(p, sm, pc.cur.b, item_stage<MODE>(pc.cur, pc.cur.L, pc.k), pc.page, pc.issued % SM::kNumStages);
   pc.issued++;
   if (++pc.k >= pc.nst) {  // items always have at least one stage
     pc.item++;
@@ -475,10 +488,15 @@ __device__ void producer_advance(const DecodeParams& p, DecodeSmem& sm, ProdCurs
   pc.page = stage_page<MODE>(p, pc.cur, pc.k);
 }
 
-template <int MODE>
+template <int MODE, int NH>
 __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(DecodeParams p) {
+  static_assert(NH == 16 || NH == 32, "16 or 32 heads per CTA");
+  using SM = DecodeSmem<NH>;
+  constexpr int kS = SM::kNumStages;
+  constexpr int NP = NH / 16;                       // 16-head halves sharing each unpack
+  constexpr uint32_t kTmemA = tmem_a_col<NH>();
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
+  SM& sm = *reinterpret_cast<SM*>(smem_raw);
   const int cta = blockIdx.y;
   pdl_wait();  // the plan
   pdl_launch_dependents();
@@ -489,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int r = lane >> 2, i = lane & 3;
   const int hb_idx = blockIdx.x;
-  const int h0 = hb_idx * 16;
+  const int h0 = hb_idx * NH;
   const int H = p.H;
   constexpr int CB = token_bytes(MODE);
   constexpr int CBITS = content_bits(MODE);
@@ -497,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
   constexpr int ROPE_OFF = 8 * GBYTES;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&sm.full[s], 1);
+    for (int s = 0; s < kS; ++s) mbar_init(&sm.full[s], 1);
     for (int s = 0; s < kAggBufs; ++s) mbar_init(&sm.agg_done[s], kWarps);
     fence_mbar_init();
     fence_proxy_async();
@@ -512,13 +530,15 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
   const uint32_t tmem = sm.tmem_base;
   int agg_ctr = 0;    // aggregation steps issued by this CTA
   int page_ctr = -1;  // the last of them that was a page step (reads every A column)
-  constexpr uint32_t kAggIdesc = umma_idesc_f16(128, 16);
+  constexpr uint32_t kAggIdesc = umma_idesc_f16(128, NH);
   ProdCursor pc;
   if (tid == 0) {
     producer_init<MODE>(p, pc, first, i0, i1);
-    for (int s = 0; s < kStages; ++s) producer_advance<MODE>(p, sm, pc, i1);
+    for (int s = 0; s < kS; ++s) producer_advance<MODE>(p, sm, pc, i1);
   }
 
+  // query fragments of heads h0 .. h0 + 15 (those of heads h0 + 16 .. h0 + 31
+  // live in shared memory, one row of words per thread)
   uint32_t qf[2][4][2][2], qr[2][2], kmn[2];
   int cur_b = -1;
   const int hh = 4 * w + (lane >> 3);  // reducer lanes: head hh, tokens tp, tp+1
@@ -527,66 +547,210 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
   bool failed = false;
   int g_fail = 0;
 
+  // Query fragments (B operand of the score MMA: k = channel, n = head) of
+  // heads h0 + hoff .. h0 + hoff + 15, with the per-group query sums of the
+  // min-term MMA.
+  auto make_q_frags = [&](int b, int hoff, uint32_t (&QF)[2][4][2][2], uint32_t (&QR)[2][2], uint32_t (&KM)[2]) {
+    float k2[3][2];
+    const uint16_t* ql = p.q_latent + ((size_t)b * H + h0) * kDL;
+    const uint16_t* qp = p.q_rope + ((size_t)b * H + h0) * kDR;
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+      const int h = hoff + 8 * hb + r;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float acc = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const int c = 64 * (2 * w + j) + 16 * kk + 2 * i;
+          QF[j][kk][hb][0] = bf2_to_h2(*reinterpret_cast<const uint32_t*>(ql + (size_t)h * kDL + c));
+          QF[j][kk][hb][1] = bf2_to_h2(*reinterpret_cast<const uint32_t*>(ql + (size_t)h * kDL + c + 8));
+          const float2 a = __half22float2(u32_as_h2(QF[j][kk][hb][0]));
+          const float2 bq = __half22float2(u32_as_h2(QF[j][kk][hb][1]));
+          acc += (a.x + a.y) + (bq.x + bq.y);
+        }
+        k2[j][hb] = acc;
+      }
+      const int c = 16 * w + 2 * i;
+      QR[hb][0] = bf2_to_h2(*reinterpret_cast<const uint32_t*>(qp + (size_t)h * kDR + c));
+      QR[hb][1] = bf2_to_h2(*reinterpret_cast<const uint32_t*>(qp + (size_t)h * kDR + c + 8));
+      const float2 a = __half22float2(u32_as_h2(QR[hb][0]));
+      const float2 bq = __half22float2(u32_as_h2(QR[hb][1]));
+      k2[2][hb] = (a.x + a.y) + (bq.x + bq.y);
+    }
+#pragma unroll
+    for (int j = 0; j < 3; ++j)
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        float v = k2[j][hb];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        k2[j][hb] = v;
+      }
+    // B fragment of the min-term MMA: rows k = 2j, 2j+1 hold hi/lo of K2_j.
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+      const float v = (i == 0) ? k2[0][hb] : (i == 1) ? k2[1][hb] : k2[2][hb];
+      const __half hi = __float2half_rn(v);
+      const __half lo = __float2half_rn(v - __half2float(hi));
+      KM[hb] = (i < 3) ? h2_as_u32(__halves2half2(hi, lo)) : 0u;
+    }
+  };
+  // The second half's fragments: 38 words per thread, as 10 uint4 rows
+  // [row][thread] (each thread reads back only its own words).
+  auto store_q_frags = [&](const uint32_t (&QF)[2][4][2][2], const uint32_t (&QR)[2][2], const uint32_t (&KM)[2]) {
+    if constexpr (NP == 2) {
+      uint32_t wv[40];
+      const uint32_t* f = &QF[0][0][0][0];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) wv[k] = f[k];
+      wv[32] = QR[0][0];
+      wv[33] = QR[0][1];
+      wv[34] = QR[1][0];
+      wv[35] = QR[1][1];
+      wv[36] = KM[0];
+      wv[37] = KM[1];
+      wv[38] = wv[39] = 0u;
+#pragma unroll
+      for (int k = 0; k < 10; ++k)
+        sm.qx[k * kThreads + tid] = make_uint4(wv[4 * k], wv[4 * k + 1], wv[4 * k + 2], wv[4 * k + 3]);
+    }
+  };
+  auto load_q_frags = [&](uint32_t (&QF)[2][4][2][2], uint32_t (&QR)[2][2], uint32_t (&KM)[2]) {
+    if constexpr (NP == 2) {
+      uint32_t wv[40];
+#pragma unroll
+      for (int k = 0; k < 10; ++k) {
+        const uint4 v = sm.qx[k * kThreads + tid];
+        wv[4 * k] = v.x;
+        wv[4 * k + 1] = v.y;
+        wv[4 * k + 2] = v.z;
+        wv[4 * k + 3] = v.w;
+      }
+      uint32_t* f = &QF[0][0][0][0];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) f[k] = wv[k];
+      QR[0][0] = wv[32];
+      QR[0][1] = wv[33];
+      QR[1][0] = wv[34];
+      QR[1][1] = wv[35];
+      KM[0] = wv[36];
+      KM[1] = wv[37];
+    }
+  };
+
+  // Lazy-max rescale of O^T: the columns of head h times alpha[h], on this
+  // warp's 32 lanes of every block (no aggregation MMA may be in flight).
+  auto rescale_o = [&]() {
+    float al[NH];
+#pragma unroll
+    for (int h = 0; h < NH; ++h) al[h] = sm.alpha[h];
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk)
+#pragma unroll
+      for (int hp = 0; hp < NP; ++hp) {
+        uint32_t v[16];
+        const uint32_t ta = tmem + ((uint32_t)(32 * w) << 16) + (uint32_t)(NH * blk + 16 * hp);
+        tmem_ld_32x32b_x16(ta, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 16; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * al[16 * hp + h]);
+        tmem_st_32x32b_x16(ta, v);
+      }
+    tmem_wait_st();
+  };
+  // Partial scores of this warp's channels (content groups 2w, 2w+1 and RoPE
+  // channels 16w .. 16w+15) for 16 tokens (rows r, r + 8 of the fragments)
+  // and heads hoff .. hoff + 15, published to sp[w][head][tcol + token].
+  auto score_pass = [&](const uint32_t (&mx)[3], const uint32_t (&my)[3], const uint32_t (&ch)[2][4][4],
+                        const uint32_t (&rf)[4], const uint32_t (&QF)[2][4][2][2], const uint32_t (&QR)[2][2],
+                        const uint32_t (&KM)[2], int hoff, int tcol) {
+    float sacc[2][4];  // S[t][h] for the two 8-head tiles
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[hb][e] = 0.f;
+    // min term: S += [mn_j (hi, lo) rows] . [K2_j hi, lo]
+    {
+      uint32_t a[4];
+      const uint32_t mnx = (i == 0) ? mx[0] : (i == 1) ? mx[1] : mx[2];
+      const uint32_t mny = (i == 0) ? my[0] : (i == 1) ? my[1] : my[2];
+      a[0] = (i < 3) ? __byte_perm(mnx, 0, 0x3232) : 0u;  // (mn, mn)
+      a[1] = (i < 3) ? __byte_perm(mny, 0, 0x3232) : 0u;
+      a[2] = 0u;
+      a[3] = 0u;
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) mma16816(sacc[hb], a, KM[hb], 0u);
+    }
+    // scale terms: D_j = codes_j . Q_j per group; the two content-group
+    // chains are interleaved.
+    {
+      float d0[2][4], d1[2][4], d2[2][4];
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d0[hb][e] = d1[hb][e] = d2[hb][e] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        mma16816(d0[0], ch[0][kk], QF[0][kk][0][0], QF[0][kk][0][1]);
+        mma16816(d1[0], ch[1][kk], QF[1][kk][0][0], QF[1][kk][0][1]);
+        mma16816(d0[1], ch[0][kk], QF[0][kk][1][0], QF[0][kk][1][1]);
+        mma16816(d1[1], ch[1][kk], QF[1][kk][1][0], QF[1][kk][1][1]);
+      }
+      mma16816(d2[0], rf, QR[0][0], QR[0][1]);
+      mma16816(d2[1], rf, QR[1][0], QR[1][1]);
+      float sxv[3], syv[3];
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        sxv[j] = __half2float(__ushort_as_half((unsigned short)(mx[j] & 0xffffu)));
+        syv[j] = __half2float(__ushort_as_half((unsigned short)(my[j] & 0xffffu)));
+      }
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        sacc[hb][0] = fmaf(sxv[2], d2[hb][0], fmaf(sxv[1], d1[hb][0], fmaf(sxv[0], d0[hb][0], sacc[hb][0])));
+        sacc[hb][1] = fmaf(sxv[2], d2[hb][1], fmaf(sxv[1], d1[hb][1], fmaf(sxv[0], d0[hb][1], sacc[hb][1])));
+        sacc[hb][2] = fmaf(syv[2], d2[hb][2], fmaf(syv[1], d1[hb][2], fmaf(syv[0], d0[hb][2], sacc[hb][2])));
+        sacc[hb][3] = fmaf(syv[2], d2[hb][3], fmaf(syv[1], d1[hb][3], fmaf(syv[0], d0[hb][3], sacc[hb][3])));
+      }
+    }
+    // publish partial scores: sacc[hb] = S[t = r (e 0,1) / r+8 (e 2,3)][h = 8hb + 2i (+1)]
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+      const int h = hoff + 8 * hb + 2 * i;
+      const int t = tcol + r;
+      sm.sp[w][h][t] = sacc[hb][0];
+      sm.sp[w][h + 1][t] = sacc[hb][1];
+      sm.sp[w][h][t + 8] = sacc[hb][2];
+      sm.sp[w][h + 1][t + 8] = sacc[hb][3];
+    }
+  };
+
   for (int item_idx = i0; item_idx < i1; ++item_idx) {
     const Item it = p.items[item_idx];
     const int L = it.L;
     const bool single = p.item_start[it.b + 1] - p.item_start[it.b] == 1;
     if (it.b != cur_b) {
       cur_b = it.b;
-      // query fragments (B operand of the score MMA: k = channel, n = head)
-      float k2[3][2];
-      const uint16_t* ql = p.q_latent + ((size_t)it.b * H + h0) * kDL;
-      const uint16_t* qp = p.q_rope + ((size_t)it.b * H + h0) * kDR;
-#pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
-        const int h = 8 * hb + r;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          float acc = 0.f;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const int c = 64 * (2 * w + j) + 16 * kk + 2 * i;
-            qf[j][kk][hb][0] = bf2_to_h2(*reinterpret_cast<const uint32_t*>(ql + (size_t)h * kDL + c));
-            qf[j][kk][hb][1] = bf2_to_h2(*reinterpret_cast<const uint32_t*>(ql + (size_t)h * kDL + c + 8));
-            const float2 a = __half22float2(u32_as_h2(qf[j][kk][hb][0]));
-            const float2 bq = __half22float2(u32_as_h2(qf[j][kk][hb][1]));
-            acc += (a.x + a.y) + (bq.x + bq.y);
-          }
-          k2[j][hb] = acc;
-        }
-        const int c = 16 * w + 2 * i;
-        qr[hb][0] = bf2_to_h2(*reinterpret_cast<const uint32_t*>(qp + (size_t)h * kDR + c));
-        qr[hb][1] = bf2_to_h2(*reinterpret_cast<const uint32_t*>(qp + (size_t)h * kDR + c + 8));
-        const float2 a = __half22float2(u32_as_h2(qr[hb][0]));
-        const float2 bq = __half22float2(u32_as_h2(qr[hb][1]));
-        k2[2][hb] = (a.x + a.y) + (bq.x + bq.y);
-      }
-#pragma unroll
-      for (int j = 0; j < 3; ++j)
-#pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {
-          float v = k2[j][hb];
-          v += __shfl_xor_sync(0xffffffffu, v, 1);
-          v += __shfl_xor_sync(0xffffffffu, v, 2);
-          k2[j][hb] = v;
-        }
-      // B fragment of the min-term MMA: rows k = 2j, 2j+1 hold hi/lo of K2_j.
-#pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
-        const float v = (i == 0) ? k2[0][hb] : (i == 1) ? k2[1][hb] : k2[2][hb];
-        const __half hi = __float2half_rn(v);
-        const __half lo = __float2half_rn(v - __half2float(hi));
-        kmn[hb] = (i < 3) ? h2_as_u32(__halves2half2(hi, lo)) : 0u;
+      make_q_frags(it.b, 0, qf, qr, kmn);
+      if constexpr (NP == 2) {
+        uint32_t q1f[2][4][2][2], q1r[2][2], q1k[2];
+        make_q_frags(it.b, 16, q1f, q1r, q1k);
+        store_q_frags(q1f, q1r, q1k);
       }
     }
 
     bool item_first = true;  // the item's first aggregation MMA overwrites O^T
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run[NP], l_run[NP];  // per 16-head half: heads hh (+ 16)
+#pragma unroll
+    for (int hp = 0; hp < NP; ++hp) {
+      m_run[hp] = -INFINITY;
+      l_run[hp] = 0.f;
+    }
 
     const int nst = item_stages<MODE>(it, L);
     for (int k = 0; k < nst && !failed; ++k) {
-      const int buf = g % kStages;
-      const bool ok = mbar_wait_bounded(&sm.full[buf], (g / kStages) & 1, kWaitLimit);
+      const int buf = g % kS;
+      const bool ok = mbar_wait_bounded(&sm.full[buf], (g / kS) & 1, kWaitLimit);
       g++;
       const uint8_t* st = sm.stage[buf];
       const bool bad = sm.stage_bad[buf] != 0;
@@ -612,11 +776,6 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
         uint32_t mx[3], my[3];  // meta (s, mn) of tokens r (x) and r+8 (y), groups 2w, 2w+1, rope
         uint32_t ch[2][4][4];   // fp16 A fragments of the content tile (exact codes, later dequantized)
         uint32_t rf[4];
-        float sacc[2][4];       // S[t][h] for head blocks 0/1
-#pragma unroll
-        for (int hb = 0; hb < 2; ++hb)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sacc[hb][e] = 0.f;
         if (packed_s) {
           const uint8_t* mtab = st + page_code_bytes(MODE);
 #pragma unroll
@@ -698,57 +857,11 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
           rf[2] = v0 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(rx + e1)) : 0u;
           rf[3] = v1 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(ry + e1)) : 0u;
         }
-        // min term: S += [mn_j (hi, lo) rows] . [K2_j hi, lo]
-        {
-          uint32_t a[4];
-          const uint32_t mnx = (i == 0) ? mx[0] : (i == 1) ? mx[1] : mx[2];
-          const uint32_t mny = (i == 0) ? my[0] : (i == 1) ? my[1] : my[2];
-          a[0] = (i < 3) ? __byte_perm(mnx, 0, 0x3232) : 0u;  // (mn, mn)
-          a[1] = (i < 3) ? __byte_perm(mny, 0, 0x3232) : 0u;
-          a[2] = 0u;
-          a[3] = 0u;
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb) mma16816(sacc[hb], a, kmn[hb], 0u);
-        }
-        // scale terms: D_j = codes_j . Q_j per group; the two content-group
-        // chains are interleaved, Q fragments come from the shared table.
-        {
-          float d0[2][4], d1[2][4], d2[2][4];
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) d0[hb][e] = d1[hb][e] = d2[hb][e] = 0.f;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            mma16816(d0[0], ch[0][kk], qf[0][kk][0][0], qf[0][kk][0][1]);
-            mma16816(d1[0], ch[1][kk], qf[1][kk][0][0], qf[1][kk][0][1]);
-            mma16816(d0[1], ch[0][kk], qf[0][kk][1][0], qf[0][kk][1][1]);
-            mma16816(d1[1], ch[1][kk], qf[1][kk][1][0], qf[1][kk][1][1]);
-          }
-          mma16816(d2[0], rf, qr[0][0], qr[0][1]);
-          mma16816(d2[1], rf, qr[1][0], qr[1][1]);
-          float sxv[3], syv[3];
-#pragma unroll
-          for (int j = 0; j < 3; ++j) {
-            sxv[j] = __half2float(__ushort_as_half((unsigned short)(mx[j] & 0xffffu)));
-            syv[j] = __half2float(__ushort_as_half((unsigned short)(my[j] & 0xffffu)));
-          }
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb) {
-            sacc[hb][0] = fmaf(sxv[2], d2[hb][0], fmaf(sxv[1], d1[hb][0], fmaf(sxv[0], d0[hb][0], sacc[hb][0])));
-            sacc[hb][1] = fmaf(sxv[2], d2[hb][1], fmaf(sxv[1], d1[hb][1], fmaf(sxv[0], d0[hb][1], sacc[hb][1])));
-            sacc[hb][2] = fmaf(syv[2], d2[hb][2], fmaf(syv[1], d1[hb][2], fmaf(syv[0], d0[hb][2], sacc[hb][2])));
-            sacc[hb][3] = fmaf(syv[2], d2[hb][3], fmaf(syv[1], d1[hb][3], fmaf(syv[0], d0[hb][3], sacc[hb][3])));
-          }
-        }
-        // publish partial scores: sacc[hb] = S[t = r (e 0,1) / r+8 (e 2,3)][h = 8hb + 2i (+1)]
-#pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {
-          const int h = 8 * hb + 2 * i;
-          sm.sp[w][h][r] = sacc[hb][0];
-          sm.sp[w][h + 1][r] = sacc[hb][1];
-          sm.sp[w][h][r + 8] = sacc[hb][2];
-          sm.sp[w][h + 1][r + 8] = sacc[hb][3];
+        score_pass(mx, my, ch, rf, qf, qr, kmn, 0, 0);
+        if constexpr (NP == 2) {
+          uint32_t q1f[2][4][2][2], q1r[2][2], q1k[2];
+          load_q_frags(q1f, q1r, q1k);
+          score_pass(mx, my, ch, rf, q1f, q1r, q1k, 16, 0);
         }
         // dequantize the content tile in place (fp16, one rounding) and
         // transpose each 8x8 block for the aggregation B operand.
@@ -790,45 +903,48 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
         // the stage's shared memory is no longer read: refill it with the
         // next stage of the CTA's stream
         if (tid == 0 && s == nsteps - 1) producer_advance<MODE>(p, sm, pc, i1);
-        // ---------------- online softmax for head hh, tokens tp, tp+1
+        // ---------------- online softmax for heads hh (+ 16), tokens tp, tp+1
         {
-          float x0 = 0.f, x1 = 0.f;
-#pragma unroll
-          for (int ww = 0; ww < kWarps; ++ww) {
-            const float2 v = *reinterpret_cast<const float2*>(&sm.sp[ww][hh][tp]);
-            x0 += v.x;
-            x1 += v.y;
-          }
           const bool ok0 = FULL || (!bad & (all_in | row_valid<MODE>(sref, s * kT + tp, L)));
           const bool ok1 = FULL || (!bad & (all_in | row_valid<MODE>(sref, s * kT + tp + 1, L)));
-          x0 = ok0 ? x0 * p.scale_log2 : -INFINITY;
-          x1 = ok1 ? x1 * p.scale_log2 : -INFINITY;
-          // Lazy rescale: keep a stale running max while every P <= 2^8. The
-          // tile max (three shuffles) is only needed when some score exceeds
-          // it by more than 8 (log2 units), e.g. on an item's first tile.
-          float alpha = 1.f;
-          if (__any_sync(0xffffffffu, fmaxf(x0, x1) > m_run + 8.f)) {
-            float tmax = fmaxf(x0, x1);
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
-            const bool upd = tmax > m_run + 8.f;  // m_run = -inf gives alpha = 0
-            alpha = upd ? ex2(m_run - tmax) : 1.f;
-            m_run = upd ? tmax : m_run;
-          }
-          const float mref = (m_run == -INFINITY) ? 0.f : m_run;  // nothing valid yet: x = -inf -> p = 0
-          const float p0 = ex2(x0 - mref), p1 = ex2(x1 - mref);
-          l_run = l_run * alpha + (p0 + p1);
-          {
-            // P^T[head hh][k] with token k order matching the TMEM A columns
-            const int kp = tp < 8 ? 2 * tp : 2 * tp - 14;
-            const int off = (hh >> 3) * 256 + (kp >> 3) * 128 + (hh & 7) * 16 + (kp & 7) * 2;
+          const int kp = tp < 8 ? 2 * tp : 2 * tp - 14;  // P^T token order matching the TMEM A columns
+          bool rs = false;
+#pragma unroll
+          for (int hp = 0; hp < NP; ++hp) {
+            const int hq = hh + 16 * hp;
+            float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+            for (int ww = 0; ww < kWarps; ++ww) {
+              const float2 v = *reinterpret_cast<const float2*>(&sm.sp[ww][hq][tp]);
+              x0 += v.x;
+              x1 += v.y;
+            }
+            x0 = ok0 ? x0 * p.scale_log2 : -INFINITY;
+            x1 = ok1 ? x1 * p.scale_log2 : -INFINITY;
+            // Lazy rescale: keep a stale running max while every P <= 2^8. The
+            // tile max (three shuffles) is only needed when some score exceeds
+            // it by more than 8 (log2 units), e.g. on an item's first tile.
+            float alpha = 1.f;
+            if (__any_sync(0xffffffffu, fmaxf(x0, x1) > m_run[hp] + 8.f)) {
+              float tmax = fmaxf(x0, x1);
+              tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+              tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+              tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+              const bool upd = tmax > m_run[hp] + 8.f;  // m_run = -inf gives alpha = 0
+              alpha = upd ? ex2(m_run[hp] - tmax) : 1.f;
+              m_run[hp] = upd ? tmax : m_run[hp];
+            }
+            const float mref = (m_run[hp] == -INFINITY) ? 0.f : m_run[hp];  // nothing valid yet: p = 0
+            const float p0 = ex2(x0 - mref), p1 = ex2(x1 - mref);
+            l_run[hp] = l_run[hp] * alpha + (p0 + p1);
+            const int off = (hq >> 3) * 256 + (kp >> 3) * 128 + (hq & 7) * 16 + (kp & 7) * 2;
             *reinterpret_cast<__half2*>(&sm.pt[ab][off]) = __floats2half2_rn(p0, p1);
-            fence_view_async_shared();
-            const bool any_rs = __any_sync(0xffffffffu, alpha != 1.f);
-            if (lane == 0) sm.rescale_flag[w] = any_rs;
+            if ((lane & 7) == 0) sm.alpha[hq] = alpha;
+            rs |= alpha != 1.f;
           }
-          if ((lane & 7) == 0) sm.alpha[hh] = alpha;
+          fence_view_async_shared();
+          const bool any_rs = __any_sync(0xffffffffu, rs);
+          if (lane == 0) sm.rescale_flag[w] = any_rs;
         }
         named_bar_sync(2, kThreads);
         // ---------------- aggregation
@@ -839,20 +955,7 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
             const int lp = agg_ctr - 1;
             mbar_wait_bounded(&sm.agg_done[lp % kAggBufs], (lp / kAggBufs) & 1, kWaitLimit);
             tc_fence_after();
-            float al[16];
-#pragma unroll
-            for (int h = 0; h < 16; ++h) al[h] = sm.alpha[h];
-#pragma unroll
-            for (int blk = 0; blk < 4; ++blk) {
-              uint32_t v[16];
-              const uint32_t ta = tmem + ((uint32_t)(32 * w) << 16) + (uint32_t)(16 * blk);
-              tmem_ld_32x32b_x16(ta, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int h = 0; h < 16; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * al[h]);
-              tmem_st_32x32b_x16(ta, v);
-            }
-            tmem_wait_st();
+            rescale_o();
             tc_fence_before();
             named_bar_sync(3, kThreads);
             tc_fence_after();
@@ -860,7 +963,7 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
           if (lane == 0) {
             tc_fence_after();
             const uint64_t bdesc = umma_smem_desc(smem_u32(sm.pt[ab]), 128, 256);
-            umma_f16_ts(tmem + (uint32_t)(16 * w), tmem + (uint32_t)(kTmemA + 32 * ab + 8 * w), bdesc, kAggIdesc,
+            umma_f16_ts(tmem + (uint32_t)(NH * w), tmem + (uint32_t)(kTmemA + 32 * ab + 8 * w), bdesc, kAggIdesc,
                         !item_first);
             umma_commit(&sm.agg_done[ab]);
           }
@@ -951,59 +1054,11 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
             rf[2] = int4_pos(ax, 0u, 1);
             rf[3] = int4_pos(ay, 0u, 1);
           }
-          float sacc[2][4];
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sacc[hb][e] = 0.f;
-          {
-            uint32_t a[4];
-            const uint32_t mnx = (i == 0) ? mx[0] : (i == 1) ? mx[1] : mx[2];
-            const uint32_t mny = (i == 0) ? my[0] : (i == 1) ? my[1] : my[2];
-            a[0] = (i < 3) ? __byte_perm(mnx, 0, 0x3232) : 0u;
-            a[1] = (i < 3) ? __byte_perm(mny, 0, 0x3232) : 0u;
-            a[2] = 0u;
-            a[3] = 0u;
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb) mma16816(sacc[hb], a, kmn[hb], 0u);
-          }
-          {
-            float d0[2][4], d1[2][4], d2[2][4];
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) d0[hb][e] = d1[hb][e] = d2[hb][e] = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              mma16816(d0[0], ch[0][kk], qf[0][kk][0][0], qf[0][kk][0][1]);
-              mma16816(d1[0], ch[1][kk], qf[1][kk][0][0], qf[1][kk][0][1]);
-              mma16816(d0[1], ch[0][kk], qf[0][kk][1][0], qf[0][kk][1][1]);
-              mma16816(d1[1], ch[1][kk], qf[1][kk][1][0], qf[1][kk][1][1]);
-            }
-            mma16816(d2[0], rf, qr[0][0], qr[0][1]);
-            mma16816(d2[1], rf, qr[1][0], qr[1][1]);
-            float sxv[3], syv[3];
-#pragma unroll
-            for (int j = 0; j < 3; ++j) {
-              sxv[j] = __half2float(__ushort_as_half((unsigned short)(mx[j] & 0xffffu)));
-              syv[j] = __half2float(__ushort_as_half((unsigned short)(my[j] & 0xffffu)));
-            }
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {
-              sacc[hb][0] = fmaf(sxv[2], d2[hb][0], fmaf(sxv[1], d1[hb][0], fmaf(sxv[0], d0[hb][0], sacc[hb][0])));
-              sacc[hb][1] = fmaf(sxv[2], d2[hb][1], fmaf(sxv[1], d1[hb][1], fmaf(sxv[0], d0[hb][1], sacc[hb][1])));
-              sacc[hb][2] = fmaf(syv[2], d2[hb][2], fmaf(syv[1], d1[hb][2], fmaf(syv[0], d0[hb][2], sacc[hb][2])));
-              sacc[hb][3] = fmaf(syv[2], d2[hb][3], fmaf(syv[1], d1[hb][3], fmaf(syv[0], d0[hb][3], sacc[hb][3])));
-            }
-          }
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb) {
-            const int h = 8 * hb + 2 * i;
-            const int t = 16 * sub + r;
-            sm.sp[w][h][t] = sacc[hb][0];
-            sm.sp[w][h + 1][t] = sacc[hb][1];
-            sm.sp[w][h][t + 8] = sacc[hb][2];
-            sm.sp[w][h + 1][t + 8] = sacc[hb][3];
+          score_pass(mx, my, ch, rf, qf, qr, kmn, 0, 16 * sub);
+          if constexpr (NP == 2) {
+            uint32_t q1f[2][4][2][2], q1r[2][2], q1k[2];
+            load_q_frags(q1f, q1r, q1k);
+            score_pass(mx, my, ch, rf, q1f, q1r, q1k, 16, 16 * sub);
           }
           // dequantize, transpose, and store the sub-step's A tile in TMEM
           // (lanes = channels, columns = token pairs)
@@ -1031,83 +1086,76 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
         // barrier 1: partial scores and A tiles complete; agrees on a timed-out wait
         if (named_bar_or(1, kThreads, !(ok && agg_ok))) return true;
         if (tid == 0) producer_advance<MODE>(p, sm, pc, i1);
-        // online softmax for head hh, tokens tq .. tq + 7 (sub-step tq / 16)
+        // online softmax for heads hh (+ 16), tokens tq .. tq + 7 (sub-step tq / 16)
         {
           const int tq = 8 * (lane & 7);
-          float x[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) x[u] = 0.f;
-#pragma unroll
-          for (int ww = 0; ww < kWarps; ++ww) {
-            const float4 v0 = *reinterpret_cast<const float4*>(&sm.sp[ww][hh][tq]);
-            const float4 v1 = *reinterpret_cast<const float4*>(&sm.sp[ww][hh][tq + 4]);
-            x[0] += v0.x;
-            x[1] += v0.y;
-            x[2] += v0.z;
-            x[3] += v0.w;
-            x[4] += v1.x;
-            x[5] += v1.y;
-            x[6] += v1.z;
-            x[7] += v1.w;
-          }
-          float xm = -INFINITY;
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            bool valid = true;
-            if constexpr (MASKED) {
-              const int t = kPage * sref.idx + tq + u;
-              valid = (t >= kSink) & (t < L - kRecent);
-            }
-            x[u] = valid ? x[u] * p.scale_log2 : -INFINITY;
-            xm = fmaxf(xm, x[u]);
-          }
-          float alpha = 1.f;
-          if (__any_sync(0xffffffffu, xm > m_run + 8.f)) {
-            float tmax = xm;
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
-            const bool upd = tmax > m_run + 8.f;
-            alpha = upd ? ex2(m_run - tmax) : 1.f;
-            m_run = upd ? tmax : m_run;
-          }
-          float psum = 0.f;
           const int sub = tq >> 4;
-          const float mref = (MASKED && m_run == -INFINITY) ? 0.f : m_run;  // nothing valid yet: p = 0
+          bool rs = false;
 #pragma unroll
-          for (int u = 0; u < 8; u += 2) {
-            const float pa = ex2(x[u] - mref), pb = ex2(x[u + 1] - mref);
-            psum += pa + pb;
-            const int t = (tq & 15) + u;              // token pair t, t + 1 of the sub-step
-            const int kp = t < 8 ? 2 * t : 2 * t - 14;  // their K index in the TMEM A columns
-            const int off = (hh >> 3) * 256 + (kp >> 3) * 128 + (hh & 7) * 16 + (kp & 7) * 2;
-            *reinterpret_cast<__half2*>(&sm.ptp[sub][off]) = __floats2half2_rn(pa, pb);
+          for (int hp = 0; hp < NP; ++hp) {
+            const int hq = hh + 16 * hp;
+            float x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) x[u] = 0.f;
+#pragma unroll
+            for (int ww = 0; ww < kWarps; ++ww) {
+              const float4 v0 = *reinterpret_cast<const float4*>(&sm.sp[ww][hq][tq]);
+              const float4 v1 = *reinterpret_cast<const float4*>(&sm.sp[ww][hq][tq + 4]);
+              x[0] += v0.x;
+              x[1] += v0.y;
+              x[2] += v0.z;
+              x[3] += v0.w;
+              x[4] += v1.x;
+              x[5] += v1.y;
+              x[6] += v1.z;
+              x[7] += v1.w;
+            }
+            float xm = -INFINITY;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              bool valid = true;
+              if constexpr (MASKED) {
+                const int t = kPage * sref.idx + tq + u;
+                valid = (t >= kSink) & (t < L - kRecent);
+              }
+              x[u] = valid ? x[u] * p.scale_log2 : -INFINITY;
+              xm = fmaxf(xm, x[u]);
+            }
+            float alpha = 1.f;
+            if (__any_sync(0xffffffffu, xm > m_run[hp] + 8.f)) {
+              float tmax = xm;
+              tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+              tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+              tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+              const bool upd = tmax > m_run[hp] + 8.f;
+              alpha = upd ? ex2(m_run[hp] - tmax) : 1.f;
+              m_run[hp] = upd ? tmax : m_run[hp];
+            }
+            float psum = 0.f;
+            const float mref = (MASKED && m_run[hp] == -INFINITY) ? 0.f : m_run[hp];  // nothing valid yet: p = 0
+#pragma unroll
+            for (int u = 0; u < 8; u += 2) {
+              const float pa = ex2(x[u] - mref), pb = ex2(x[u + 1] - mref);
+              psum += pa + pb;
+              const int t = (tq & 15) + u;              // token pair t, t + 1 of the sub-step
+              const int kp = t < 8 ? 2 * t : 2 * t - 14;  // their K index in the TMEM A columns
+              const int off = (hq >> 3) * 256 + (kp >> 3) * 128 + (hq & 7) * 16 + (kp & 7) * 2;
+              *reinterpret_cast<__half2*>(&sm.ptp[sub][off]) = __floats2half2_rn(pa, pb);
+            }
+            l_run[hp] = l_run[hp] * alpha + psum;
+            if ((lane & 7) == 0) sm.alpha[hq] = alpha;
+            rs |= alpha != 1.f;
           }
-          l_run = l_run * alpha + psum;
           fence_view_async_shared();
-          const bool any_rs = __any_sync(0xffffffffu, alpha != 1.f);
+          const bool any_rs = __any_sync(0xffffffffu, rs);
           if (lane == 0) sm.rescale_flag[w] = any_rs;
-          if ((lane & 7) == 0) sm.alpha[hh] = alpha;
         }
         named_bar_sync(2, kThreads);
         {
           const bool need_rs = !item_first && (sm.rescale_flag[0] | sm.rescale_flag[1] | sm.rescale_flag[2] |
                                                sm.rescale_flag[3]);
           if (need_rs) {  // rare (lazy max): scale O^T columns by alpha[head]; no MMA is in flight
-            float al[16];
-#pragma unroll
-            for (int h = 0; h < 16; ++h) al[h] = sm.alpha[h];
-#pragma unroll
-            for (int blk = 0; blk < 4; ++blk) {
-              uint32_t v[16];
-              const uint32_t ta = tmem + ((uint32_t)(32 * w) << 16) + (uint32_t)(16 * blk);
-              tmem_ld_32x32b_x16(ta, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int h = 0; h < 16; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * al[h]);
-              tmem_st_32x32b_x16(ta, v);
-            }
-            tmem_wait_st();
+            rescale_o();
             tc_fence_before();
             named_bar_sync(3, kThreads);
             tc_fence_after();
@@ -1117,7 +1165,7 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
 #pragma unroll
             for (int sub = 0; sub < 4; ++sub) {
               const uint64_t bdesc = umma_smem_desc(smem_u32(sm.ptp[sub]), 128, 256);
-              umma_f16_ts(tmem + (uint32_t)(16 * w), tmem + (uint32_t)(kTmemA + 32 * sub + 8 * w), bdesc,
+              umma_f16_ts(tmem + (uint32_t)(NH * w), tmem + (uint32_t)(kTmemA + 32 * sub + 8 * w), bdesc,
                           kAggIdesc, !item_first || sub > 0);
             }
             umma_commit(&sm.agg_done[agg_ctr % kAggBufs]);
@@ -1163,14 +1211,17 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
       }
     }
 
-    // ---- item epilogue: normalized partial O and lse for heads h0..h0+15
-    float l_tot = l_run;
-    l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
-    l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
-    l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 4);
-    if ((lane & 7) == 0) {
-      sm.fin_m[hh] = m_run;
-      sm.fin_l[hh] = failed ? 0.f : l_tot;
+    // ---- item epilogue: normalized partial O and lse for heads h0 .. h0 + NH - 1
+#pragma unroll
+    for (int hp = 0; hp < NP; ++hp) {
+      float l_tot = l_run[hp];
+      l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
+      l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
+      l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 4);
+      if ((lane & 7) == 0) {
+        sm.fin_m[hh + 16 * hp] = m_run[hp];
+        sm.fin_l[hh + 16 * hp] = failed ? 0.f : l_tot;
+      }
     }
     __syncthreads();
     // A sequence with a single item is final here (bf16 out, lse); otherwise
@@ -1183,31 +1234,35 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
         mbar_wait_bounded(&sm.agg_done[lp % kAggBufs], (lp / kAggBufs) & 1, kWaitLimit);
       }
       tc_fence_after();
-      float inv[16];
-#pragma unroll
-      for (int h = 0; h < 16; ++h) {
-        const float l = sm.fin_l[h];
-        inv[h] = l > 0.f ? 1.f / l : 0.f;
-      }
       const int x = lane;
 #pragma unroll
-      for (int blk = 0; blk < 4; ++blk) {
-        uint32_t v[16];
-        tmem_ld_32x32b_x16(tmem + ((uint32_t)(32 * w) << 16) + (uint32_t)(16 * blk), v);
-        tmem_wait_ld();
-        const int c = 128 * w + 64 * (blk >> 1) + 16 * (2 * (blk & 1) + (x >> 4)) + (x & 15);
+      for (int hp = 0; hp < NP; ++hp) {
+        float inv[16];
 #pragma unroll
         for (int h = 0; h < 16; ++h) {
-          const float val = inv[h] != 0.f ? __uint_as_float(v[h]) * inv[h] : 0.f;
-          if (single)
-            p.out[((size_t)it.b * H + h0 + h) * kDL + c] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
-          else
-            op[(size_t)h * kDL + c] = __float2half_rn(val);
+          const float l = sm.fin_l[16 * hp + h];
+          inv[h] = l > 0.f ? 1.f / l : 0.f;
+        }
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk) {
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(tmem + ((uint32_t)(32 * w) << 16) + (uint32_t)(NH * blk + 16 * hp), v);
+          tmem_wait_ld();
+          const int c = 128 * w + 64 * (blk >> 1) + 16 * (2 * (blk & 1) + (x >> 4)) + (x & 15);
+#pragma unroll
+          for (int h = 0; h < 16; ++h) {
+            const int hq = 16 * hp + h;
+            const float val = inv[h] != 0.f ? __uint_as_float(v[h]) * inv[h] : 0.f;
+            if (single)
+              p.out[((size_t)it.b * H + h0 + hq) * kDL + c] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+            else
+              op[(size_t)hq * kDL + c] = __float2half_rn(val);
+          }
         }
       }
       tc_fence_before();
     }
-    if (tid < 16) {
+    if (tid < NH) {
       const float l = sm.fin_l[tid];
       const float lse_v = l > 0.f ? (sm.fin_m[tid] + log2f(l)) * 0.69314718055994531f : -INFINITY;
       if (single)
@@ -1222,7 +1277,7 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
     atomicOr(p.status, MLAQ_DEV_TIMEOUT);
     // wait (bounded) for copies still in flight before the CTA exits
     for (int gg = g_fail; gg < pc.issued; ++gg)
-      mbar_wait_bounded(&sm.full[gg % kStages], (gg / kStages) & 1, kWaitLimit);
+      mbar_wait_bounded(&sm.full[gg % kS], (gg / kS) & 1, kWaitLimit);
   }
   // every aggregation MMA has completed (waited for in each item epilogue)
   tc_fence_before();
@@ -1243,21 +1298,21 @@ constexpr int kCombineChunks = 16;  // 32-channel chunks of a head block
 __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
   const int tid = threadIdx.x;
   const int hc = tid >> 3, c4 = (tid & 7) * 4;  // head in the block, 4 channels of the chunk
-  const int units = p.B * p.HB * kCombineChunks;
+  const int units = p.B * (p.H / 16) * kCombineChunks;
   // The item ranges come from the plan, which completed before the decode
   // grid started (and so before this grid was launched): they are read
   // before waiting for the decode grid.
   int u = blockIdx.x;
   int s0 = 0, s1 = 0;
   if (u < units) {
-    const int b = (u / kCombineChunks) / p.HB;
+    const int b = (u / kCombineChunks) / (p.H / 16);
     s0 = p.item_start[b];
     s1 = p.item_start[b + 1];
   }
   pdl_wait();
   for (; u < units; u += gridDim.x) {
     const int chunk = u % kCombineChunks, rest = u / kCombineChunks;
-    const int hb = rest % p.HB, b = rest / p.HB;
+    const int hb = rest % (p.H / 16), b = rest / (p.H / 16);
     if (u != (int)blockIdx.x) {
       s0 = p.item_start[b];
       s1 = p.item_start[b + 1];
@@ -1332,9 +1387,9 @@ static cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, si
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-template <int MODE>
+template <int MODE, int NH>
 static cudaError_t run_decode(mlaq_cache* c, const DecodeParams& p, int grid_cta, cudaStream_t s) {
-  const int smem = (int)sizeof(DecodeSmem);
+  const int smem = (int)sizeof(DecodeSmem<NH>);
   // Opt in to >48 KB of dynamic shared memory once per device (the first call
   // on a device must not be inside a stream capture).
   static bool attr_done[kMaxDevices] = {};
@@ -1342,16 +1397,16 @@ static cudaError_t run_decode(mlaq_cache* c, const DecodeParams& p, int grid_cta
   cudaError_t ea = cudaGetDevice(&dev);
   if (ea != cudaSuccess) return ea;
   if (dev < 0 || dev >= kMaxDevices || !attr_done[dev]) {
-    ea = cudaFuncSetAttribute(decode_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    ea = cudaFuncSetAttribute(decode_kernel<MODE, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (ea != cudaSuccess) return ea;
     if (dev >= 0 && dev < kMaxDevices) attr_done[dev] = true;
   }
   cudaEvent_t* ev = nullptr;
   if (c->timing_events && c->timing_n < c->timing_max)
     ev = reinterpret_cast<cudaEvent_t*>(c->timing_events) + 2 * c->timing_n;  // ev[0] precedes the plan
-  cudaError_t e = launch_pdl(decode_kernel<MODE>, dim3(p.HB, grid_cta), dim3(kThreads), smem, s, p);
+  cudaError_t e = launch_pdl(decode_kernel<MODE, NH>, dim3(p.HB, grid_cta), dim3(kThreads), smem, s, p);
   if (e == cudaSuccess) {
-    const int units = p.B * p.HB * kCombineChunks;
+    const int units = p.B * (p.H / 16) * kCombineChunks;
     e = launch_pdl(combine_kernel, dim3(max(1, min(units, 2 * c->decode_ctas))), dim3(128), 0, s, p);
   }
   if (ev) {
@@ -1366,7 +1421,9 @@ cudaError_t launch_decode(mlaq_cache* c, const uint16_t* q_latent, const uint16_
                           uint16_t* out, float* lse, cudaStream_t s) {
   char* ws = static_cast<char*>(c->workspace);
   const WsLayout lay = ws_layout(c->max_seqs, c->max_heads);
-  const int HB = H / 16;
+  // heads per CTA: 32 when H allows it (one unpack per page for both halves)
+  const int NH = H % 32 == 0 ? 32 : 16;
+  const int HB = H / NH;
   // item slots (CTAs per head block); the planner's one-pass scan over CTA
   // boundaries needs G + 1 <= 1024
   const int G = max(1, min(kMaxPlanCtas - 1, c->decode_ctas / HB));
@@ -1420,9 +1477,14 @@ cudaError_t launch_decode(mlaq_cache* c, const uint16_t* q_latent, const uint16_
                              reinterpret_cast<int*>(ws + lay.cta_item_start),
                              reinterpret_cast<Item*>(ws + lay.cta_first), reinterpret_cast<int*>(ws + kWsNumItems));
   if (e != cudaSuccess) return e;
-  if (c->mode == MLAQ_C4R4) return run_decode<MLAQ_C4R4>(c, p, G, s);
-  if (c->mode == MLAQ_C2R4) return run_decode<MLAQ_C2R4>(c, p, G, s);
-  return run_decode<MLAQ_BF16>(c, p, G, s);
+  if (NH == 32) {
+    if (c->mode == MLAQ_C4R4) return run_decode<MLAQ_C4R4, 32>(c, p, G, s);
+    if (c->mode == MLAQ_C2R4) return run_decode<MLAQ_C2R4, 32>(c, p, G, s);
+    return run_decode<MLAQ_BF16, 32>(c, p, G, s);
+  }
+  if (c->mode == MLAQ_C4R4) return run_decode<MLAQ_C4R4, 16>(c, p, G, s);
+  if (c->mode == MLAQ_C2R4) return run_decode<MLAQ_C2R4, 16>(c, p, G, s);
+  return run_decode<MLAQ_BF16, 16>(c, p, G, s);
 }
 
 size_t workspace_bytes_for(int max_seqs, int max_heads) { return ws_layout(max_seqs, max_heads).total; }
