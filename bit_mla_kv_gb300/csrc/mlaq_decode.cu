@@ -1407,7 +1407,9 @@ static cudaError_t run_decode(mlaq_cache* c, const DecodeParams& p, int grid_cta
   cudaError_t e = launch_pdl(decode_kernel<MODE, NH>, dim3(p.HB, grid_cta), dim3(kThreads), smem, s, p);
   if (e == cudaSuccess) {
     const int units = p.B * (p.H / 16) * kCombineChunks;
-    e = launch_pdl(combine_kernel, dim3(max(1, min(units, 2 * c->decode_ctas))), dim3(128), 0, s, p);
+    // one unit per CTA: every unit's partial loads are one round trip, and the
+    // units of unsplit sequences end at once
+    e = launch_pdl(combine_kernel, dim3(max(1, units)), dim3(128), 0, s, p);
   }
   if (ev) {
     cudaEventRecord(ev[1], s);

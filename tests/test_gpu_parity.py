@@ -81,14 +81,21 @@ def test_decode_edge_lengths(mode):
         assert_close_out(out[b], lse[b], ro, rl, f"{mode} L={L}")
 
 
-@pytest.mark.parametrize("H", [32, 128])
-def test_decode_more_heads(H):
-    case = Case("C4R4", [5, 140, 777, 2048], H, seed=14)
+@pytest.mark.parametrize("mode,H", [("C4R4", 32), ("C4R4", 48), ("C4R4", 64), ("C4R4", 128), ("C2R4", 64),
+                                    ("BF16", 64)])
+def test_decode_more_heads(mode, H):
+    # 32 heads per CTA when H is a multiple of 32 (one head block at H=32,
+    # two at 64, four at 128), 16 otherwise (three blocks at H=48); forced
+    # single-item and many-item splits exercise the final and partial epilogues.
+    case = Case(mode, [5, 140, 777, 2048], H, seed=14)
     case.build()
-    out, lse = case.decode()
-    for b in range(case.B):
-        ro, rl = case.oracle_seq(b)
-        assert_close_out(out[b], lse[b], ro, rl, f"H={H} seq {b}")
+    for ctas in (None, 1, 600):
+        if ctas is not None:
+            case.cache.set_decode_ctas(ctas)
+        out, lse = case.decode()
+        for b in range(case.B):
+            ro, rl = case.oracle_seq(b)
+            assert_close_out(out[b], lse[b], ro, rl, f"{mode} H={H} ctas={ctas} seq {b}")
 
 
 @pytest.mark.parametrize("mode", ["C4R4", "C2R4", "BF16"])
