@@ -1291,79 +1291,94 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
 // Combine (split-KV): for every sequence with more than one item, the
 // normalized partials O_k and their lse_k merge into
 //   out = sum_k exp(lse_k - M) O_k / sum_k exp(lse_k - M),  lse = M + log(sum_k exp(lse_k - M)).
-// One work unit = (sequence, head block, 64-channel chunk); a thread owns one
-// head and 8 channels, so all partials of a unit are read in one batch.
-constexpr int kCombineBatch = 16;
-constexpr int kCombineChunks = 16;  // 32-channel chunks of a head block
+// One work unit = (sequence, 16-head block, chunk of 8 CPT channels); a thread
+// owns one head and CPT channels and reads BATCH partials per round trip.
+// CPT = 4 with BATCH = 16 reads a sequence split up to 16 ways in one round
+// trip; CPT = 16 with BATCH = 4 serves large batches with a quarter of the
+// CTAs (one wave where the small units would need several).
+template <int CPT, int BATCH>
 __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
+  constexpr int kChunks = kDL / (8 * CPT);
+  constexpr int NV = CPT / 4;  // uint2 (4 fp16) words per partial
   const int tid = threadIdx.x;
-  const int hc = tid >> 3, c4 = (tid & 7) * 4;  // head in the block, 4 channels of the chunk
-  const int units = p.B * (p.H / 16) * kCombineChunks;
+  const int hc = tid >> 3, cq = (tid & 7) * CPT;  // head in the block, channels of the chunk
+  const int HB16 = p.H / 16;
+  const int units = p.B * HB16 * kChunks;
   // The item ranges come from the plan, which completed before the decode
   // grid started (and so before this grid was launched): they are read
   // before waiting for the decode grid.
   int u = blockIdx.x;
   int s0 = 0, s1 = 0;
   if (u < units) {
-    const int b = (u / kCombineChunks) / (p.H / 16);
+    const int b = (u / kChunks) / HB16;
     s0 = p.item_start[b];
     s1 = p.item_start[b + 1];
   }
   pdl_wait();
   for (; u < units; u += gridDim.x) {
-    const int chunk = u % kCombineChunks, rest = u / kCombineChunks;
-    const int hb = rest % (p.H / 16), b = rest / (p.H / 16);
+    const int chunk = u % kChunks, rest = u / kChunks;
+    const int hb = rest % HB16, b = rest / HB16;
     if (u != (int)blockIdx.x) {
       s0 = p.item_start[b];
       s1 = p.item_start[b + 1];
     }
     if (s1 - s0 < 2) continue;  // finalized by the decode kernel
     const int row = 16 * hb + hc;
-    const int c = (kDL / kCombineChunks) * chunk + c4;
-    // one pass over the partials, kCombineBatch at a time, with a running max
+    const int c = 8 * CPT * chunk + cq;
+    // one pass over the partials, BATCH at a time, with a running max
     float m = -INFINITY, tot = 0.f;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int k0 = s0; k0 < s1; k0 += kCombineBatch) {
-      uint2 v[kCombineBatch];
-      float l[kCombineBatch];
+    float acc[CPT];
 #pragma unroll
-      for (int k = 0; k < kCombineBatch; ++k) {
+    for (int e = 0; e < CPT; ++e) acc[e] = 0.f;
+    for (int k0 = s0; k0 < s1; k0 += BATCH) {
+      uint2 v[BATCH][NV];
+      float l[BATCH];
+#pragma unroll
+      for (int k = 0; k < BATCH; ++k) {
         const bool in = k0 + k < s1;
         l[k] = in ? __ldcg(&p.lse_part[(size_t)(k0 + k) * p.H + row]) : -INFINITY;
-        v[k] = in ? __ldcg(reinterpret_cast<const uint2*>(p.o_part + ((size_t)(k0 + k) * p.H + row) * kDL + c))
-                  : make_uint2(0u, 0u);
+        const uint2* src = reinterpret_cast<const uint2*>(p.o_part + ((size_t)(k0 + k) * p.H + row) * kDL + c);
+#pragma unroll
+        for (int q = 0; q < NV; ++q) v[k][q] = in ? __ldcg(src + q) : make_uint2(0u, 0u);
       }
       float mb = m;
 #pragma unroll
-      for (int k = 0; k < kCombineBatch; ++k) mb = fmaxf(mb, l[k]);
+      for (int k = 0; k < BATCH; ++k) mb = fmaxf(mb, l[k]);
       if (mb == -INFINITY) continue;  // no tokens so far
       const float sc = expf(m - mb);  // 0 while m = -inf
       tot *= sc;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[e] *= sc;
+      for (int e = 0; e < CPT; ++e) acc[e] *= sc;
 #pragma unroll
-      for (int k = 0; k < kCombineBatch; ++k) {
+      for (int k = 0; k < BATCH; ++k) {
         const float wgt = expf(l[k] - mb);  // 0 for padding (lse = -inf)
         tot += wgt;
-        const __half2* hv = reinterpret_cast<const __half2*>(&v[k]);
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float2 f = __half22float2(hv[e]);
-          acc[2 * e] = fmaf(wgt, f.x, acc[2 * e]);
-          acc[2 * e + 1] = fmaf(wgt, f.y, acc[2 * e + 1]);
+        for (int q = 0; q < NV; ++q) {
+          const __half2* hv = reinterpret_cast<const __half2*>(&v[k][q]);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float2 f = __half22float2(hv[e]);
+            acc[4 * q + 2 * e] = fmaf(wgt, f.x, acc[4 * q + 2 * e]);
+            acc[4 * q + 2 * e + 1] = fmaf(wgt, f.y, acc[4 * q + 2 * e + 1]);
+          }
         }
       }
       m = mb;
     }
     const float inv = tot > 0.f ? 1.f / tot : 0.f;
-    uint2 pk;
-    uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
+    uint2* dst = reinterpret_cast<uint2*>(p.out + ((size_t)b * p.H + row) * kDL + c);
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const __nv_bfloat162 bv = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
-      pw[e] = *reinterpret_cast<const uint32_t*>(&bv);
+    for (int q = 0; q < NV; ++q) {
+      uint2 pk;
+      uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const __nv_bfloat162 bv = __floats2bfloat162_rn(acc[4 * q + 2 * e] * inv, acc[4 * q + 2 * e + 1] * inv);
+        pw[e] = *reinterpret_cast<const uint32_t*>(&bv);
+      }
+      dst[q] = pk;
     }
-    *reinterpret_cast<uint2*>(p.out + ((size_t)b * p.H + row) * kDL + c) = pk;
     if (chunk == 0 && (tid & 7) == 0) p.lse[(size_t)b * p.H + row] = tot > 0.f ? m + logf(tot) : -INFINITY;
   }
 }
@@ -1406,10 +1421,13 @@ static cudaError_t run_decode(mlaq_cache* c, const DecodeParams& p, int grid_cta
     ev = reinterpret_cast<cudaEvent_t*>(c->timing_events) + 2 * c->timing_n;  // ev[0] precedes the plan
   cudaError_t e = launch_pdl(decode_kernel<MODE, NH>, dim3(p.HB, grid_cta), dim3(kThreads), smem, s, p);
   if (e == cudaSuccess) {
-    const int units = p.B * (p.H / 16) * kCombineChunks;
-    // one unit per CTA: every unit's partial loads are one round trip, and the
-    // units of unsplit sequences end at once
-    e = launch_pdl(combine_kernel, dim3(max(1, units)), dim3(128), 0, s, p);
+    // one unit per CTA, every unit's partial loads in one round trip; large
+    // batches take the 16-channel units so that the grid stays near one wave
+    const int small_units = p.B * (p.H / 16) * (kDL / 32);
+    if (small_units <= 16 * max(1, c->num_sms))
+      e = launch_pdl(combine_kernel<4, 16>, dim3(max(1, small_units)), dim3(128), 0, s, p);
+    else
+      e = launch_pdl(combine_kernel<16, 4>, dim3(max(1, small_units / 4)), dim3(128), 0, s, p);
   }
   if (ev) {
     cudaEventRecord(ev[1], s);
