@@ -1086,10 +1086,10 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
         // barrier 1: partial scores and A tiles complete; agrees on a timed-out wait
         if (named_bar_or(1, kThreads, !(ok && agg_ok))) return true;
         if (tid == 0) producer_advance<MODE>(p, sm, pc, i1);
-        // online softmax for heads hh (+ 16), tokens tq .. tq + 7 (sub-step tq / 16)
+        // online softmax for heads hh (+ 16), tokens tq .. tq + 3 and 32 + tq .. 32 + tq + 3
+        // (a quarter warp reads 128 contiguous bytes of a score row)
         {
-          const int tq = 8 * (lane & 7);
-          const int sub = tq >> 4;
+          const int tq = 4 * (lane & 7);
           bool rs = false;
 #pragma unroll
           for (int hp = 0; hp < NP; ++hp) {
@@ -1100,7 +1100,7 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
 #pragma unroll
             for (int ww = 0; ww < kWarps; ++ww) {
               const float4 v0 = *reinterpret_cast<const float4*>(&sm.sp[ww][hq][tq]);
-              const float4 v1 = *reinterpret_cast<const float4*>(&sm.sp[ww][hq][tq + 4]);
+              const float4 v1 = *reinterpret_cast<const float4*>(&sm.sp[ww][hq][tq + 32]);
               x[0] += v0.x;
               x[1] += v0.y;
               x[2] += v0.z;
@@ -1115,7 +1115,7 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
             for (int u = 0; u < 8; ++u) {
               bool valid = true;
               if constexpr (MASKED) {
-                const int t = kPage * sref.idx + tq + u;
+                const int t = kPage * sref.idx + tq + (u < 4 ? u : 28 + u);
                 valid = (t >= kSink) & (t < L - kRecent);
               }
               x[u] = valid ? x[u] * p.scale_log2 : -INFINITY;
@@ -1137,7 +1137,8 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
             for (int u = 0; u < 8; u += 2) {
               const float pa = ex2(x[u] - mref), pb = ex2(x[u + 1] - mref);
               psum += pa + pb;
-              const int t = (tq & 15) + u;              // token pair t, t + 1 of the sub-step
+              const int tp64 = tq + (u < 4 ? u : 28 + u);  // token pair tp64, tp64 + 1 of the page
+              const int sub = tp64 >> 4, t = tp64 & 15;
               const int kp = t < 8 ? 2 * t : 2 * t - 14;  // their K index in the TMEM A columns
               const int off = (hq >> 3) * 256 + (kp >> 3) * 128 + (hq & 7) * 16 + (kp & 7) * 2;
               *reinterpret_cast<__half2*>(&sm.ptp[sub][off]) = __floats2half2_rn(pa, pb);
