@@ -48,6 +48,41 @@ def test_writer_codes_meta_ring_bit_exact(mode):
         np.testing.assert_array_equal(ring[b][valid], er[valid], err_msg=f"ring seq {b} L={L}")
 
 
+@pytest.mark.parametrize("mode", ["C4R4", "C2R4"])
+def test_writer_exact_ties_round_half_to_even(mode):
+    # Groups with a power-of-two scale whose values sit on code midpoints, so
+    # (x - mn) / s = k + 1/2 exactly and the code must round half to even like
+    # the oracle's fp32 quantizer; 1000 rows in one call take the bulk writer.
+    case = Case(mode, [700, 300], 16, seed=31)
+    n = sum(case.seq_lens)
+    rng = np.random.default_rng(31)
+    c = np.empty((n, 512), np.float32)
+    k = np.empty((n, 64), np.float32)
+    for arr, bits in ((c, 4 if mode == "C4R4" else 2), (k, 4)):
+        qmax = (1 << bits) - 1
+        for g in range(arr.shape[1] // 64):
+            s0 = rng.choice([0.25, 0.5, 1.0], size=n)
+            mn = rng.integers(-4, 4, size=n) * 0.5
+            vals = rng.integers(0, qmax, size=(n, 64)) + 0.5
+            exact = rng.random((n, 64)) < 0.25  # some entries exactly on a code
+            vals[exact] = np.floor(vals[exact])
+            vals[:, 0] = 0.0   # the group minimum
+            vals[:, 1] = qmax  # the group maximum: s = s0 exactly
+            arr[:, 64 * g:64 * g + 64] = mn[:, None] + vals * s0[:, None]
+    case.c = torch.from_numpy(c).to(torch.bfloat16)
+    case.k = torch.from_numpy(k).to(torch.bfloat16)
+    assert np.array_equal(case.c.float().numpy(), c) and np.array_equal(case.k.float().numpy(), k)
+    case.build()
+    assert case.cache.device_status() == 0
+    codes, meta = _export_all(case)
+    off = 0
+    for b, L in enumerate(case.seq_lens):
+        ec, em = expected_codes(case, b)
+        np.testing.assert_array_equal(codes[off:off + L], ec, err_msg=f"codes seq {b}")
+        np.testing.assert_array_equal(meta[off:off + L].view(np.uint16), em.view(np.uint16), err_msg=f"meta seq {b}")
+        off += L
+
+
 def test_writer_bf16_pages_hold_tokens():
     case = Case("BF16", [1, 64, 65, 300], 16, seed=12)
     case.build()
