@@ -139,6 +139,19 @@ int mlaq_decode(mlaq_cache* c, const uint16_t* q_latent, const uint16_t* q_rope,
   return e == cudaSuccess ? MLAQ_OK : MLAQ_ERR_CUDA;
 }
 
+int mlaq_decode_mtp(mlaq_cache* c, const uint16_t* q_latent, const uint16_t* q_rope, const int32_t* page_table,
+                    const int32_t* seq_lens, int32_t B, int32_t Q, int32_t H, float softmax_scale,
+                    uint16_t* out_latent, float* lse, struct CUstream_st* stream) {
+  if (!c || !q_latent || !q_rope || !page_table || !seq_lens || !out_latent || !lse) return MLAQ_ERR_NULL;
+  if (B <= 0 || Q <= 0 || H < 16 || H % 16 || Q * H > 128) return MLAQ_ERR_SHAPE;
+  if (B > c->max_seqs || Q * H > c->max_heads) return MLAQ_ERR_CAPACITY;
+  if (!aligned16(q_latent) || !aligned16(q_rope) || !aligned16(out_latent)) return MLAQ_ERR_ALIGN;
+  // the Q query rows of a sequence are laid out as Q * H heads
+  cudaError_t e = launch_decode(c, q_latent, q_rope, page_table, seq_lens, B, Q * H, softmax_scale, out_latent, lse,
+                                reinterpret_cast<cudaStream_t>(stream), Q);
+  return e == cudaSuccess ? MLAQ_OK : MLAQ_ERR_CUDA;
+}
+
 int mlaq_decode_noalloc(int mode, const void* codes, const void* meta, const void* ring, int32_t num_pages,
                         int32_t max_pages_per_seq, const uint16_t* q_latent, const uint16_t* q_rope,
                         const int32_t* page_table, const int32_t* seq_lens, int32_t B, int32_t H,

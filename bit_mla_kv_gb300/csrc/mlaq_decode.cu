@@ -78,6 +78,7 @@ struct DecodeParams {
   uint16_t* out;
   float* lse;
   int B, H, HB, max_pages, num_pages, max_tokens;
+  int q_len, h_per_q;  // query tokens per sequence; heads per query token (H = q_len * h_per_q)
   float scale_log2;
 };
 
@@ -410,6 +411,16 @@ __device__ __forceinline__ bool row_valid(const StageRef& st, int j, int L) {
   const bool page = (t64 >= kSink) & (t64 < L - kRecent);
   const bool quarter = t16 < L;
   return st.kind == 0 ? ring : (st.kind == 1 ? page : quarter);
+}
+
+// Position of the token in row j of a stage (valid rows only): ring slot j < 4
+// holds sink token j, slot 4 + r the newest token t < L with t mod 128 == r.
+template <int MODE>
+__device__ __forceinline__ int row_token(const StageRef& st, int j, int L) {
+  if (st.kind == 1) return kPage * st.idx + j;
+  const int slot = kT * st.idx + j;
+  if (st.kind == 2) return slot;
+  return slot < kSink ? slot : L - 1 - ((L - 1 - (slot - kSink)) % kRecent);
 }
 
 // Producer: issue the bulk copies of a stage into buffer `buf`.
@@ -912,6 +923,12 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
 #pragma unroll
           for (int hp = 0; hp < NP; ++hp) {
             const int hq = hh + 16 * hp;
+            bool ok0h = ok0, ok1h = ok1;
+            if (p.q_len > 1) {  // query j of several sees t < L - (q_len - 1 - j)
+              const int lim = L - (p.q_len - 1 - (h0 + hq) / p.h_per_q);
+              ok0h = ok0h && row_token<MODE>(sref, s * kT + tp, L) < lim;
+              ok1h = ok1h && row_token<MODE>(sref, s * kT + tp + 1, L) < lim;
+            }
             float x0 = 0.f, x1 = 0.f;
 #pragma unroll
             for (int ww = 0; ww < kWarps; ++ww) {
@@ -919,8 +936,8 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
               x0 += v.x;
               x1 += v.y;
             }
-            x0 = ok0 ? x0 * p.scale_log2 : -INFINITY;
-            x1 = ok1 ? x1 * p.scale_log2 : -INFINITY;
+            x0 = ok0h ? x0 * p.scale_log2 : -INFINITY;
+            x1 = ok1h ? x1 * p.scale_log2 : -INFINITY;
             // Lazy rescale: keep a stale running max while every P <= 2^8. The
             // tile max (three shuffles) is only needed when some score exceeds
             // it by more than 8 (log2 units), e.g. on an item's first tile.
@@ -1439,7 +1456,7 @@ static cudaError_t run_decode(mlaq_cache* c, const DecodeParams& p, int grid_cta
 
 cudaError_t launch_decode(mlaq_cache* c, const uint16_t* q_latent, const uint16_t* q_rope,
                           const int32_t* page_table, const int32_t* seq_lens, int B, int H, float scale,
-                          uint16_t* out, float* lse, cudaStream_t s) {
+                          uint16_t* out, float* lse, cudaStream_t s, int q_len) {
   char* ws = static_cast<char*>(c->workspace);
   const WsLayout lay = ws_layout(c->max_seqs, c->max_heads);
   // heads per CTA: 32 when H allows it (one unpack per page for both halves)
@@ -1469,6 +1486,8 @@ cudaError_t launch_decode(mlaq_cache* c, const uint16_t* q_latent, const uint16_
   p.B = B;
   p.H = H;
   p.HB = HB;
+  p.q_len = q_len;
+  p.h_per_q = H / q_len;
   p.max_pages = c->max_pages_per_seq;
   p.num_pages = c->num_pages;
   p.max_tokens = c->max_pages_per_seq * kPage;

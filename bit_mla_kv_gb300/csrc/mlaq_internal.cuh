@@ -333,5 +333,5 @@ cudaError_t launch_export(const mlaq_cache* c, const int32_t* page_table, int B,
                           const int32_t* token_t, int n, uint8_t* codes_out, uint16_t* meta_out, cudaStream_t s);
 cudaError_t launch_decode(mlaq_cache* c, const uint16_t* q_latent, const uint16_t* q_rope,
                           const int32_t* page_table, const int32_t* seq_lens, int B, int H, float scale,
-                          uint16_t* out, float* lse, cudaStream_t s);
+                          uint16_t* out, float* lse, cudaStream_t s, int q_len = 1);
 }  // namespace mlaq

@@ -34,7 +34,7 @@ EXPORTED = [
     "mlaq_buffer_sizes", "mlaq_cache_create", "mlaq_cache_destroy", "mlaq_append", "mlaq_decode",
     "mlaq_export_tokens", "mlaq_cache_bytes", "mlaq_get_device_status", "mlaq_clear_device_status",
     "mlaq_timing_enable", "mlaq_timing_read", "mlaq_set_decode_ctas", "mlaq_status_string",
-    "mlaq_decode_noalloc", "mlaq_debug_wait_probe",
+    "mlaq_decode_noalloc", "mlaq_debug_wait_probe", "mlaq_decode_mtp",
 ]
 
 _lib.mlaq_status_string.restype = ctypes.c_char_p
@@ -55,6 +55,7 @@ _lib.mlaq_set_decode_ctas.argtypes = [_vp, _i32]
 _lib.mlaq_decode_noalloc.argtypes = [ctypes.c_int, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _i32,
                                      ctypes.c_float, _vp, _vp, _vp, _vp]
 _lib.mlaq_debug_wait_probe.argtypes = [_vp, _i32, _i32, _vp]
+_lib.mlaq_decode_mtp.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, ctypes.c_float, _vp, _vp, _vp]
 for _name in EXPORTED:
     if _name != "mlaq_status_string":
         getattr(_lib, _name).restype = ctypes.c_int
@@ -202,6 +203,25 @@ class Cache:
         _need(lse, torch.float32, (B, H), "lse")
         _check(_lib.mlaq_decode(self._h, _ptr(q_latent), _ptr(q_rope), _ptr(page_table), _ptr(seq_lens), B, H,
                                 float(softmax_scale), _ptr(out), _ptr(lse), _stream(stream)), "mlaq_decode")
+        return out, lse
+
+    def decode_mtp(self, q_latent, q_rope, page_table, seq_lens, softmax_scale, out=None, lse=None, stream=None):
+        """Decode attention for Q query tokens per sequence, causal over the Q
+        newest tokens (query j sees t < L - (Q - 1 - j)); q_latent [B, Q, H, 512],
+        q_rope [B, Q, H, 64]; returns (out [B, Q, H, 512] bf16, lse [B, Q, H] fp32)."""
+        B, Q, H = q_latent.shape[0], q_latent.shape[1], q_latent.shape[2]
+        _need(q_latent, torch.bfloat16, (B, Q, H, 512), "q_latent")
+        _need(q_rope, torch.bfloat16, (B, Q, H, 64), "q_rope")
+        _need(page_table, torch.int32, (B, self.max_pages_per_seq), "page_table")
+        _need(seq_lens, torch.int32, (B,), "seq_lens")
+        if out is None:
+            out = torch.empty(B, Q, H, 512, dtype=torch.bfloat16, device=q_latent.device)
+        if lse is None:
+            lse = torch.empty(B, Q, H, dtype=torch.float32, device=q_latent.device)
+        _need(out, torch.bfloat16, (B, Q, H, 512), "out")
+        _need(lse, torch.float32, (B, Q, H), "lse")
+        _check(_lib.mlaq_decode_mtp(self._h, _ptr(q_latent), _ptr(q_rope), _ptr(page_table), _ptr(seq_lens), B, Q, H,
+                                    float(softmax_scale), _ptr(out), _ptr(lse), _stream(stream)), "mlaq_decode_mtp")
         return out, lse
 
     def export_tokens(self, page_table, token_b, token_t, stream=None):

@@ -160,6 +160,23 @@ int mlaq_decode(mlaq_cache* cache, const uint16_t* q_latent, const uint16_t* q_r
                 float softmax_scale, uint16_t* out_latent, float* lse,
                 struct CUstream_st* stream);
 
+/* Decode attention for Q query tokens per sequence (multi-token prediction
+ * or speculative verification; the pages describe Q = 1, this is its causal
+ * extension). The Q new tokens must already be appended: seq_lens[b] = L
+ * counts them, and query j = 0..Q-1 (position L - Q + j) attends to tokens
+ * t < L - (Q - 1 - j), each in the representation (BF16 or packed) that the
+ * length-L cache gives it, under one softmax per query.
+ *   q_latent [B, Q, H, 512] bf16, q_rope [B, Q, H, 64] bf16;
+ *   out_latent [B, Q, H, 512] bf16, lse [B, Q, H] fp32.
+ * Q >= 1, H a multiple of 16, Q * H <= 128 and <= the cache's max_heads (the
+ * Q * H query rows share every unpacked page, as heads do). A query that sees
+ * no token gets out = 0, lse = -inf. Same launches, status and capture rules
+ * as mlaq_decode; Q = 1 is mlaq_decode. Returns MLAQ_ERR_SHAPE or
+ * MLAQ_ERR_CAPACITY for sizes outside those bounds. */
+int mlaq_decode_mtp(mlaq_cache* cache, const uint16_t* q_latent, const uint16_t* q_rope,
+                    const int32_t* page_table, const int32_t* seq_lens, int32_t B, int32_t Q, int32_t H,
+                    float softmax_scale, uint16_t* out_latent, float* lse, struct CUstream_st* stream);
+
 /* Allocation-free variant of mlaq_decode. The pages describe no such call;
  * it exists for callers that cannot allocate device memory: code running
  * inside another runtime's allocator, plugins that may not call cudaMalloc

@@ -30,6 +30,10 @@ Readings taken where the pages are silent:
       log of the sum of exp(score); out = sum_t softmax_t * c_t (512-d latent).
   R6  every token gets a packed copy (sink and recent ones too); the ring slot
       of a non-sink token t is 4 + (t mod 128); sink token t uses slot t.
+  R7  several query tokens per sequence (the pages describe one): with Q new
+      tokens appended (length L), query j = 0..Q-1 attends to tokens
+      t < L - (Q - 1 - j), causally, and every token keeps the representation
+      (BF16 or packed) that the length-L cache gives it.
 
 Parity pins for every function live in tests/test_oracle.py.
 """
@@ -217,9 +221,14 @@ def attend(q_lat, q_rope, kv, scale: float):
     return out, lse
 
 
-def decode_sequence(q_lat, q_rope, tokens_bf16, codes, meta, L, scale, mode):
-    """Decode one sequence: token selection, then one softmax (fp64)."""
+def decode_sequence(q_lat, q_rope, tokens_bf16, codes, meta, L, scale, mode, n_attend=None):
+    """Decode one sequence: token selection, then one softmax (fp64).
+
+    n_attend (reading R7): the query sees only tokens t < n_attend, each in the
+    representation the length-L cache gives it; None means all L tokens."""
     kv = assemble_kv(tokens_bf16, codes, meta, L, mode)
+    if n_attend is not None:
+        kv = kv[:max(0, min(int(n_attend), L))]
     return attend(q_lat, q_rope, kv, scale)
 
 

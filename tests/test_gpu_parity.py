@@ -133,6 +133,32 @@ def test_decode_more_heads(mode, H):
             assert_close_out(out[b], lse[b], ro, rl, f"{mode} H={H} ctas={ctas} seq {b}")
 
 
+@pytest.mark.parametrize("mode,Q,H", [("C4R4", 2, 16), ("C4R4", 4, 16), ("C2R4", 2, 32), ("BF16", 3, 16)])
+def test_decode_multi_token_causal(mode, Q, H):
+    # Q query tokens per sequence after their Q tokens were appended: query j
+    # sees t < L - (Q - 1 - j). The lengths put the hidden tokens among the
+    # sink slots (L <= 6), the recent ring and, in BF16 mode, the last page.
+    case = Case(mode, [1, 2, 3, 6, 133, 140, 700, 3000], H, seed=40 + Q)
+    case.build(max_heads=Q * H)
+    ql, qr = W.make_queries(case.B, Q * H, W.generator(90 + Q, "cpu"), "cpu")
+    ql = ql.view(case.B, Q, H, 512).contiguous()
+    qr = qr.view(case.B, Q, H, 64).contiguous()
+    for ctas in (None, 1, 600):
+        if ctas is not None:
+            case.cache.set_decode_ctas(ctas)
+        out, lse = case.cache.decode_mtp(ql.cuda(), qr.cuda(), case.pt_d, case.seq_d, case.scale)
+        assert case.cache.device_status() == 0
+        for b, L in enumerate(case.seq_lens):
+            tok = case.tokens(b)
+            codes = meta = None
+            if mode != "BF16":
+                codes, meta = O.quantize_tokens(tok[:, :512], tok[:, 512:], mode)
+            for j in range(Q):
+                ro, rl = O.decode_sequence(ql[b, j].float().numpy(), qr[b, j].float().numpy(), tok, codes, meta, L,
+                                           case.scale, mode, n_attend=L - (Q - 1 - j))
+                assert_close_out(out[b, j], lse[b, j], ro, rl, f"{mode} Q={Q} ctas={ctas} seq {b} query {j}")
+
+
 @pytest.mark.parametrize("mode", ["C4R4", "C2R4", "BF16"])
 def test_decode_running_max_rescale(mode):
     # Later tokens carry larger latents, so the running max of every head

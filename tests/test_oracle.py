@@ -302,3 +302,37 @@ def test_compression_accounting_near_published():
         ratio = ref / pol
         # our metadata is 36 B/token vs ~32 implied by the pages: within 2%
         assert abs(ratio - published) / published < 0.02, (L, ratio, published)
+
+
+def test_decode_causal_attended_prefix():
+    """Reading R7: a query that sees only tokens t < n keeps each token in the
+    representation of the length-L cache. Pinned against the selection rule
+    restated here (BF16 iff t < 4 or t >= L - 128) and the plain definition of
+    softmax attention over the chosen rows."""
+    rng = np.random.default_rng(7)
+    L = 300
+    tok = rng.standard_normal((L, 576)).astype(np.float32)
+    codes, meta = O.quantize_tokens(tok[:, :512], tok[:, 512:], "C4R4")
+    deq = O.dequantize_tokens(codes, meta)
+    ql = rng.standard_normal((2, 512))
+    qr = rng.standard_normal((2, 64))
+    scale = 1 / math.sqrt(192)
+    full = O.decode_sequence(ql, qr, tok, codes, meta, L, scale, "C4R4")
+    same = O.decode_sequence(ql, qr, tok, codes, meta, L, scale, "C4R4", n_attend=L)
+    np.testing.assert_array_equal(full[0], same[0])
+    np.testing.assert_array_equal(full[1], same[1])
+    for n in (1, 4, 5, 100, 171, 172, 173, 299):
+        rows = np.array([tok[t] if (t < 4 or t >= L - 128) else deq[t] for t in range(n)], dtype=np.float64)
+        z = scale * (ql @ rows[:, :512].T + qr @ rows[:, 512:].T)
+        w = np.exp(z - z.max(axis=1, keepdims=True))
+        want_out = (w / w.sum(axis=1, keepdims=True)) @ rows[:, :512]
+        want_lse = z.max(axis=1) + np.log(w.sum(axis=1))
+        got_out, got_lse = O.decode_sequence(ql, qr, tok, codes, meta, L, scale, "C4R4", n_attend=n)
+        np.testing.assert_allclose(got_out, want_out, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(got_lse, want_lse, rtol=1e-12, atol=1e-12)
+    # the all-BF16 cache has no selection: a prefix is a shorter sequence
+    a = O.decode_sequence(ql, qr, tok, None, None, L, scale, "BF16", n_attend=57)
+    b = O.decode_sequence(ql, qr, tok[:57], None, None, 57, scale, "BF16")
+    np.testing.assert_allclose(a[0], b[0], rtol=1e-13, atol=1e-13)
+    out0, lse0 = O.decode_sequence(ql, qr, tok, codes, meta, L, scale, "C4R4", n_attend=0)
+    assert np.all(out0 == 0) and np.all(np.isneginf(lse0))
