@@ -30,6 +30,11 @@ Readings taken where the pages are silent:
       log of the sum of exp(score); out = sum_t softmax_t * c_t (512-d latent).
   R6  every token gets a packed copy (sink and recent ones too); the ring slot
       of a non-sink token t is 4 + (t mod 128); sink token t uses slot t.
+  R8  error response (the pages' diagnosis, [AIS] "Methodology in Plain
+      English" and Main Findings): one path's cache (content latent or RoPE
+      key) gets additive noise rescaled to NMSE ||d||^2 / ||x||^2 = 0.01
+      exactly; the response is the attention output's NMSE divided by that
+      cache NMSE; the noise is an input (drawn by the caller).
   R7  several query tokens per sequence (the pages describe one): with Q new
       tokens appended (length L), query j = 0..Q-1 attends to tokens
       t < L - (Q - 1 - j), causally, and every token keeps the representation
@@ -49,7 +54,7 @@ __all__ = [
     "MODES", "mode_bits", "packed_bytes_per_token", "quantize_groups", "quantize_tokens",
     "pack_canonical", "unpack_canonical", "dequantize_tokens", "is_bf16_token",
     "bf16_token_mask", "assemble_kv", "attend", "decode_sequence", "decode_batch",
-    "combine_partials", "expected_ring", "cache_bytes",
+    "combine_partials", "expected_ring", "cache_bytes", "perturb_to_nmse", "path_response",
 ]
 
 SINK = 4            # [SLN] 方法关键点 / [ODK] 어떻게 쓰나: first 4 tokens kept in BF16
@@ -296,3 +301,32 @@ def cache_bytes(seq_lens, mode: str, page_tokens: int = 64, meta_bytes_per_token
         pol += pages * page_tokens * packed_tok + RING_SLOTS * D_QK * 2 + pages * page_entry_bytes
         ref += pages * page_tokens * D_QK * 2 + pages * page_entry_bytes
     return pol, ref
+
+
+def perturb_to_nmse(x, noise, nmse: float):
+    """x + d with d = noise rescaled so that ||d||^2 / ||x||^2 == nmse (reading R8)."""
+    x = np.asarray(x, dtype=np.float64)
+    noise = np.asarray(noise, dtype=np.float64)
+    d = noise * math.sqrt(nmse * float(np.sum(x * x)) / float(np.sum(noise * noise)))
+    return x + d
+
+
+def path_response(q_lat, q_rope, tokens, scale: float, path: str, noise, nmse: float = 0.01):
+    """Output damage per unit cache error of one path (reading R8).
+
+    tokens [L, 576] (content latent then RoPE key, full precision); path
+    'content' perturbs the latent (it enters the logits and the values),
+    'rope' the RoPE key (logits only). Returns NMSE(out') / nmse over all
+    heads of q_lat [H, 512], q_rope [H, 64]."""
+    tok = np.asarray(tokens, dtype=np.float64)
+    out, _ = attend(q_lat, q_rope, tok, scale)
+    pert = tok.copy()
+    if path == "content":
+        pert[:, :D_LATENT] = perturb_to_nmse(tok[:, :D_LATENT], noise, nmse)
+    elif path == "rope":
+        pert[:, D_LATENT:] = perturb_to_nmse(tok[:, D_LATENT:], noise, nmse)
+    else:
+        raise ValueError(path)
+    out2, _ = attend(q_lat, q_rope, pert, scale)
+    return float(np.sum((out2 - out) ** 2) / np.sum(out * out)) / nmse
+

@@ -336,3 +336,47 @@ def test_decode_causal_attended_prefix():
     np.testing.assert_allclose(a[0], b[0], rtol=1e-13, atol=1e-13)
     out0, lse0 = O.decode_sequence(ql, qr, tok, codes, meta, L, scale, "C4R4", n_attend=0)
     assert np.all(out0 == 0) and np.all(np.isneginf(lse0))
+
+
+def test_path_response_closed_forms():
+    """Reading R8 pinned by cases with closed forms: the rescaled noise has the
+    requested NMSE; with one token the softmax weight is 1, so a content
+    perturbation moves the output by exactly the cache error (response 1) and
+    a RoPE perturbation not at all (response 0); with q_rope = 0 the RoPE key
+    never reaches the output."""
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((50, 64))
+    n = rng.standard_normal((50, 64))
+    y = O.perturb_to_nmse(x, n, 0.01)
+    assert abs(np.sum((y - x) ** 2) / np.sum(x * x) - 0.01) < 1e-14
+    ql, qr = rng.standard_normal((4, 512)), rng.standard_normal((4, 64))
+    one = rng.standard_normal((1, 576))
+    assert abs(O.path_response(ql, qr, one, 0.07, "content", rng.standard_normal((1, 512))) - 1.0) < 1e-12
+    assert O.path_response(ql, qr, one, 0.07, "rope", rng.standard_normal((1, 64))) < 1e-24
+    many = rng.standard_normal((300, 576))
+    assert O.path_response(ql, np.zeros_like(qr), many, 0.07, "rope", rng.standard_normal((300, 64))) == 0.0
+
+
+def test_path_response_on_synthetic_caches():
+    """The diagnosis on the synthetic cache distribution (no model weights):
+    content and RoPE responses at cache NMSE 0.01 over whole sequences.
+    Random-data values, printed for the record; the pages' per-model numbers
+    come from trained models and are not a target."""
+    import workloads as W
+    stats = W.CacheStats(5)
+    g = W.generator(5)
+    lens = [1024, 4096]
+    c, k, cu = W.make_sequences(lens, stats, g)
+    ql, qr = W.make_queries(len(lens), 16, g)
+    rng = np.random.default_rng(5)
+    res = {"content": [], "rope": []}
+    for b, L in enumerate(lens):
+        a, e = int(cu[b]), int(cu[b + 1])
+        tok = torch.cat([c[a:e], k[a:e]], -1).float().numpy()
+        for path, width in (("content", 512), ("rope", 64)):
+            r = O.path_response(ql[b].float().numpy(), qr[b].float().numpy(), tok, W.SOFTMAX_SCALE, path,
+                                rng.standard_normal((L, width)))
+            assert np.isfinite(r) and r > 0
+            res[path].append(r)
+    rc, rr = float(np.mean(res["content"])), float(np.mean(res["rope"]))
+    print(f"synthetic caches: content response {rc:.3f}, RoPE response {rr:.3f}, ratio {rr / rc:.3f}")
