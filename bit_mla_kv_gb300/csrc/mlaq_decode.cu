@@ -938,16 +938,17 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
             }
             x0 = ok0h ? x0 * p.scale_log2 : -INFINITY;
             x1 = ok1h ? x1 * p.scale_log2 : -INFINITY;
-            // Lazy rescale: keep a stale running max while every P <= 2^8. The
-            // tile max (three shuffles) is only needed when some score exceeds
-            // it by more than 8 (log2 units), e.g. on an item's first tile.
+            // Lazy rescale: keep a stale running max while every P <= 2^14 (fp16
+            // holds it exactly enough; the sums are fp32). The tile max (three
+            // shuffles) is only needed when some score exceeds it by more than
+            // 14 (log2 units), e.g. on an item's first tile.
             float alpha = 1.f;
-            if (__any_sync(0xffffffffu, fmaxf(x0, x1) > m_run[hp] + 8.f)) {
+            if (__any_sync(0xffffffffu, fmaxf(x0, x1) > m_run[hp] + 14.f)) {
               float tmax = fmaxf(x0, x1);
               tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
               tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
               tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
-              const bool upd = tmax > m_run[hp] + 8.f;  // m_run = -inf gives alpha = 0
+              const bool upd = tmax > m_run[hp] + 14.f;  // m_run = -inf gives alpha = 0
               alpha = upd ? ex2(m_run[hp] - tmax) : 1.f;
               m_run[hp] = upd ? tmax : m_run[hp];
             }
@@ -1139,12 +1140,12 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
               xm = fmaxf(xm, x[u]);
             }
             float alpha = 1.f;
-            if (__any_sync(0xffffffffu, xm > m_run[hp] + 8.f)) {
+            if (__any_sync(0xffffffffu, xm > m_run[hp] + 14.f)) {
               float tmax = xm;
               tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
               tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
               tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
-              const bool upd = tmax > m_run[hp] + 8.f;
+              const bool upd = tmax > m_run[hp] + 14.f;
               alpha = upd ? ex2(m_run[hp] - tmax) : 1.f;
               m_run[hp] = upd ? tmax : m_run[hp];
             }
