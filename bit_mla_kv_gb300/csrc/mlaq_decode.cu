@@ -1,5 +1,5 @@
-// Split-KV MLA decode over the mixed-precision paged cache: device planner,
-// persistent attention kernel with an in-kernel log-sum-exp combine.
+// Split-KV MLA decode over the mixed-precision paged cache: a device planner,
+// a persistent attention kernel and a log-sum-exp combine kernel.
 //
 // QuantMLA (ai.info "Key Contributions" item 4; onedev.kr "어떻게 쓰나"):
 // unpack + dequant fused into attention, packed pages and metadata staged
@@ -8,29 +8,34 @@
 //
 // Work distribution. A sequence's work is a list of units: its 9 ring chunks
 // (16 BF16 sink/recent slots each) and then its packed pages (4 units each,
-// one per 16-token step); in the all-BF16 cache a unit is a 16-token quarter
-// page. The planner gives each of the G persistent CTAs an equal contiguous
-// share of the concatenated unit list, cut at page boundaries. The share of
-// one CTA inside one sequence is a work item with its own partial result;
-// the last CTA to finish a sequence merges that sequence's partials.
+// one per 16-token sub-step); in the all-BF16 cache a unit is a 16-token
+// quarter page. The planner gives each of the G persistent CTAs of a head
+// block an equal share of the concatenated unit list by a cost model, cut at
+// page boundaries. The share of one CTA inside one sequence is a work item;
+// a sequence with one item is finalized by the attention kernel, otherwise
+// the combine kernel merges its items' normalized partials.
 //
-// Attention step (one CTA = 16 heads, 4 warps, 16 tokens per step):
+// Attention (one CTA = NH = 16 or 32 heads, 4 warps, 2 CTAs per SM):
 //  * Pages (codes + fp16 meta) or ring chunks are staged by bulk copies
-//    (TMA) into a 4-deep shared-memory ring that runs ahead across items.
+//    (TMA) into a shared-memory ring (4 stages, 2 for 32-head CTAs) that runs
+//    ahead across items; every wait is bounded in wall time.
+//  * A packed page is one step of four 16-token sub-steps under one pair of
+//    barriers; ring chunks and BF16 page quarters are 16-token steps.
 //  * Warp w owns content groups 2w, 2w+1 (channels 128w..128w+127) and RoPE
 //    channels 16w..16w+15.
 //  * Scores use exact integer codes as fp16 MMA operands: per group g,
 //    D_g[t,h] = sum_{c in g} q[t,c] Q[h,c], then
 //    S[t,h] = sum_g s[t,g] D_g[t,h] + sum_g mn[t,g] sum_{c in g} Q[h,c]
 //    (the second sum is one more m16n8k16 MMA on hi/lo fp16 splits of the
-//    per-group query sums): exact up to fp32 rounding.
-//  * The four warps' partial scores meet in shared memory; each warp runs
-//    the online softmax for 4 heads (exp2, lazily rescaled max) and
-//    publishes P in fp16.
-//  * Aggregation reuses the registers: codes are dequantized once to fp16
-//    (q*s + mn, one rounding), transposed in registers with movmatrix and fed
-//    to m16n8k16 MMAs against P: O[h,c] += P[h,t] c[t,c]. The dequantized
-//    tile never touches shared memory.
+//    per-group query sums): exact up to fp32 rounding. A 32-head CTA runs
+//    this per 16-head half on the same unpacked codes.
+//  * The four warps' partial scores meet in shared memory; each thread runs
+//    the online softmax for one head (exp2, lazily rescaled max) and writes
+//    P^T in fp16 as the B operand of the aggregation.
+//  * Aggregation on tcgen05: the codes are dequantized once to fp16 (q*s +
+//    mn, one rounding), transposed in registers with movmatrix and stored to
+//    TMEM (lanes = channels); one tcgen05.mma per sub-step and channel block
+//    accumulates O^T += V^T P^T in TMEM while the warps unpack the next page.
 //  * BF16 tokens (ring and the all-BF16 cache) take the same path with
 //    (s, mn) = (1, 0).
 #include <math.h>
