@@ -222,13 +222,16 @@ int mlaq_clear_device_status(mlaq_cache* c, struct CUstream_st* stream) {
 
 int mlaq_timing_enable(mlaq_cache* c, int32_t max_calls) {
   if (!c) return MLAQ_ERR_NULL;
-  if (max_calls <= 0) return MLAQ_ERR_SHAPE;
+  if (max_calls < 0) return MLAQ_ERR_SHAPE;
   if (c->timing_events) {
     cudaEvent_t* ev = reinterpret_cast<cudaEvent_t*>(c->timing_events);
     for (int k = 0; k < 2 * c->timing_max; ++k) cudaEventDestroy(ev[k]);
     free(c->timing_events);
     c->timing_events = nullptr;
+    c->timing_max = 0;
+    c->timing_n = 0;
   }
+  if (max_calls == 0) return MLAQ_OK;  // timing off
   cudaEvent_t* ev = static_cast<cudaEvent_t*>(calloc(2 * (size_t)max_calls, sizeof(cudaEvent_t)));
   if (!ev) return MLAQ_ERR_NULL;
   for (int k = 0; k < 2 * max_calls; ++k)

@@ -230,10 +230,12 @@ int mlaq_get_device_status(mlaq_cache* cache, struct CUstream_st* stream, int32_
 int mlaq_clear_device_status(mlaq_cache* cache, struct CUstream_st* stream);
 
 /* Kernel timing for measurement: when enabled, mlaq_decode records a CUDA
- * event pair around its split-KV attention kernel (the dominant kernel) on
+ * event pair around the whole call (planner, attention and combine kernels) on
  * the call's stream, up to max_calls calls. mlaq_timing_read synchronises and
  * returns the per-call durations in milliseconds (*n = number recorded) and
- * resets the counter. Host calls; events are created at enable. */
+ * resets the counter. Host calls; events are created at enable;
+ * max_calls = 0 turns timing off (an event recorded between launches keeps
+ * the next kernel from starting before the previous one ends). */
 int mlaq_timing_enable(mlaq_cache* cache, int32_t max_calls);
 int mlaq_timing_read(mlaq_cache* cache, float* ms_out, int32_t* n);
 

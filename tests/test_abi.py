@@ -70,6 +70,7 @@ def test_host_argument_errors(lib):
     assert lib.mlaq_cache_create(ctypes.byref(out), 0, 1, 1, 1, 16, mis, mis, mis, mis, ctypes.c_size_t(0)) == -4
     assert lib.mlaq_decode(None, None, None, None, None, 1, 16, ctypes.c_float(1.0), None, None, None) == -1
     assert lib.mlaq_append(None, None, None, 1, None, None, 1, None, 0, None) == -1
+    assert lib.mlaq_timing_enable(None, 4) == -1
     # multi-token decode: Q * H <= 128, H a multiple of 16
     assert lib.mlaq_decode_mtp(None, None, None, None, None, 1, 2, 16, ctypes.c_float(1.0), None, None, None) == -1
     # the bounded-wait test hook checks its arguments before any launch
