@@ -106,7 +106,7 @@ __host__ __device__ inline int bf16_row_pos(int e, int r) { return (((e >> 3) ^ 
 //   kk = c >> 4 (MMA k-step), bi = (c >> 3) & 1 (B register b0/b1),
 //   i = (c >> 1) & 3 (thread in the quad), ln = c & 1 (fp16 lane in the pair).
 // Returns the bit offset of the code inside the group's bytes.
-__host__ __device__ inline int content_code_bit(int c, int bits) {
+__host__ __device__ constexpr int content_code_bit(int c, int bits) {
   int kk = c >> 4, bi = (c >> 3) & 1, i = (c >> 1) & 3, ln = c & 1;
   if (bits == 4) {
     int word = 2 * i + (kk >> 1);
@@ -119,7 +119,7 @@ __host__ __device__ inline int content_code_bit(int c, int bits) {
   }
 }
 // RoPE group (INT4): warp w of the decode kernel owns k-step kk = w.
-__host__ __device__ inline int rope_code_bit(int c) {
+__host__ __device__ constexpr int rope_code_bit(int c) {
   int kk = c >> 4, bi = (c >> 3) & 1, i = (c >> 1) & 3, ln = c & 1;
   int word = 2 * kk + (i >> 1);
   return word * 32 + 16 * ln + 8 * (i & 1) + 4 * bi;

@@ -83,6 +83,52 @@ def test_writer_exact_ties_round_half_to_even(mode):
         off += L
 
 
+@pytest.mark.parametrize("mode", ["C4R4", "C2R4", "BF16"])
+def test_writer_bulk_varlen_gaps_then_uniform(mode):
+    # Two bulk appends on top of each other: a varlen call whose counts
+    # include empty sequences between non-empty ones, then a uniform call of
+    # 64 rows per sequence starting at those lengths (both above the
+    # small-append threshold of 4 rows per SM).
+    first = [300, 0, 0, 517, 3, 130, 0, 64, 1, 0, 200, 63, 65, 0, 4, 700]
+    n2 = 64
+    case = Case(mode, [a + n2 for a in first], 16, seed=19)
+    from bit_mla_kv_gb300.mlaq import Cache
+    case.cache = Cache(mode, case.num_pages, case.B, case.page_table.shape[1], max_heads=16)
+    case.pt_d = case.page_table.cuda()
+    case.seq_d = torch.zeros(case.B, dtype=torch.int32, device="cuda")
+    cu0 = torch.zeros(case.B + 1, dtype=torch.int32)
+    cu0[1:] = torch.cumsum(torch.tensor(first), 0)
+    rows = torch.cat([torch.arange(int(case.cu[b]), int(case.cu[b]) + first[b]) for b in range(case.B)])
+    case.cache.append(case.pt_d, case.seq_d, case.c[rows].cuda().contiguous(), case.k[rows].cuda().contiguous(),
+                      cu_new=cu0.cuda())
+    assert case.seq_d.cpu().tolist() == first
+    rows = torch.cat([torch.arange(int(case.cu[b]) + first[b], int(case.cu[b]) + first[b] + n2)
+                      for b in range(case.B)])
+    case.cache.append(case.pt_d, case.seq_d, case.c[rows].view(case.B, n2, 512).cuda().contiguous(),
+                      case.k[rows].view(case.B, n2, 64).cuda().contiguous())
+    assert case.cache.device_status() == 0
+    assert case.seq_d.cpu().tolist() == case.seq_lens
+    if mode == "BF16":
+        pages = case.cache.bf16_pages_view().cpu()
+        for b, L in enumerate(case.seq_lens):
+            tok = torch.from_numpy(case.tokens(b))
+            for t in range(L):
+                p = int(case.page_table[b, t // 64])
+                assert torch.equal(pages[p, t % 64].float(), tok[t]), (b, t)
+        return
+    codes, meta = _export_all(case)
+    ring = case.cache.ring_view().float().cpu().numpy()
+    off = 0
+    for b, L in enumerate(case.seq_lens):
+        ec, em = expected_codes(case, b)
+        np.testing.assert_array_equal(codes[off:off + L], ec, err_msg=f"codes seq {b} L={L}")
+        np.testing.assert_array_equal(meta[off:off + L].view(np.uint16), em.view(np.uint16),
+                                      err_msg=f"meta seq {b} L={L}")
+        off += L
+        er, valid = O.expected_ring(case.tokens(b), L)
+        np.testing.assert_array_equal(ring[b][valid], er[valid], err_msg=f"ring seq {b} L={L}")
+
+
 def test_writer_bf16_pages_hold_tokens():
     case = Case("BF16", [1, 64, 65, 300], 16, seed=12)
     case.build()
