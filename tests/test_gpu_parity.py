@@ -129,6 +129,57 @@ def test_writer_bulk_varlen_gaps_then_uniform(mode):
         np.testing.assert_array_equal(ring[b][valid], er[valid], err_msg=f"ring seq {b} L={L}")
 
 
+def _extreme_groups(n, ncols, rng):
+    """Rows whose 64-channel groups stress the quantizer's edge cases: tiny
+    values (fp16-subnormal scales and minima that round), constant and
+    two-valued groups, large magnitudes and large offsets with small spread."""
+    x = np.empty((n, ncols), np.float32)
+    for g in range(ncols // 64):
+        kind = rng.integers(0, 7, size=n)
+        base = rng.standard_normal((n, 64)).astype(np.float32)
+        sc = np.ones(n, np.float32)
+        off = np.zeros(n, np.float32)
+        sc[kind == 1] = 10.0 ** rng.uniform(-8, -5, size=(kind == 1).sum())
+        off[kind == 2] = 10.0 ** rng.uniform(-6, -4.5, size=(kind == 2).sum())
+        sc[kind == 2] = 10.0 ** rng.uniform(-8, -6, size=(kind == 2).sum())
+        sc[kind == 5] = 10.0 ** rng.uniform(2, 3.8, size=(kind == 5).sum())
+        off[kind == 6] = rng.choice([-1, 1], size=(kind == 6).sum()) * 10.0 ** rng.uniform(1, 4, size=(kind == 6).sum())
+        sc[kind == 6] = 10.0 ** rng.uniform(-2, 1, size=(kind == 6).sum())
+        blk = off[:, None] + sc[:, None] * base
+        blk[kind == 3] = rng.standard_normal(((kind == 3).sum(), 1))  # constant: scale 0
+        two = kind == 4
+        a, b = rng.standard_normal(two.sum()), rng.standard_normal(two.sum())
+        blk[two] = np.where(rng.random((two.sum(), 64)) < 0.5, a[:, None], b[:, None])
+        x[:, 64 * g:64 * g + 64] = np.clip(blk, -60000, 60000)
+    return x
+
+
+@pytest.mark.parametrize("mode", ["C4R4", "C2R4"])
+@pytest.mark.parametrize("lens", [[500, 200], [60, 40, 1, 100]])
+def test_writer_extreme_groups_bit_exact(mode, lens):
+    # 700 rows take the bulk writer, 201 rows the small-append kernel; both
+    # must match the oracle's fp32 quantizer bit for bit on groups whose
+    # codes leave [0, qmax] before clamping or whose scale is an fp16
+    # subnormal or zero.
+    case = Case(mode, lens, 16, seed=41)
+    n = sum(lens)
+    rng = np.random.default_rng(41)
+    case.c = torch.from_numpy(_extreme_groups(n, 512, rng)).to(torch.bfloat16)
+    case.k = torch.from_numpy(_extreme_groups(n, 64, rng)).to(torch.bfloat16)
+    case.build()
+    assert case.cache.device_status() == 0
+    codes, meta = _export_all(case)
+    ring = case.cache.ring_view().float().cpu().numpy()
+    off = 0
+    for b, L in enumerate(case.seq_lens):
+        ec, em = expected_codes(case, b)
+        np.testing.assert_array_equal(codes[off:off + L], ec, err_msg=f"codes seq {b}")
+        np.testing.assert_array_equal(meta[off:off + L].view(np.uint16), em.view(np.uint16), err_msg=f"meta seq {b}")
+        off += L
+        er, valid = O.expected_ring(case.tokens(b), L)
+        np.testing.assert_array_equal(ring[b][valid], er[valid], err_msg=f"ring seq {b}")
+
+
 def test_writer_bf16_pages_hold_tokens():
     case = Case("BF16", [1, 64, 65, 300], 16, seed=12)
     case.build()
