@@ -92,6 +92,9 @@ int mlaq_cache_create(mlaq_cache** out, int mode, int32_t num_pages, int32_t max
   c->workspace_bytes = workspace_bytes;
   c->num_sms = sms;
   c->decode_ctas = MLAQ_CTAS_PER_SM * sms < kMaxPlanCtas ? MLAQ_CTAS_PER_SM * sms : kMaxPlanCtas;
+  c->cost_step = kDefCostStep;
+  c->cost_ring = kDefCostRing;
+  c->cost_item = kDefCostItem;
   *out = c;
   return MLAQ_OK;
 }
@@ -266,6 +269,17 @@ int mlaq_set_decode_ctas(mlaq_cache* c, int32_t ctas) {
   if (!c) return MLAQ_ERR_NULL;
   if (ctas <= 0 || ctas > kMaxPlanCtas) return MLAQ_ERR_SHAPE;
   c->decode_ctas = ctas;
+  return MLAQ_OK;
+}
+
+int mlaq_set_plan_costs(mlaq_cache* c, int32_t step, int32_t ring, int32_t item) {
+  if (!c) return MLAQ_ERR_NULL;
+  if (step < 1 || 4 * step > kPlanCostPerPage || ring < 1 || item < 0 ||
+      item + ring * ((kRing + 15) / 16) > kPlanCostRingMax)  // 9 ring chunks of 16 slots
+    return MLAQ_ERR_SHAPE;
+  c->cost_step = step;
+  c->cost_ring = ring;
+  c->cost_item = item;
   return MLAQ_OK;
 }
 

@@ -84,6 +84,7 @@ struct DecodeParams {
   float* lse;
   int B, H, HB, max_pages, num_pages, max_tokens;
   int q_len, h_per_q;  // query tokens per sequence; heads per query token (H = q_len * h_per_q)
+  int cost_step, cost_ring, cost_item;  // planning costs
   float scale_log2;
 };
 
@@ -121,25 +122,28 @@ __device__ __forceinline__ int seq_units(int mode, int L) {
   const int pages = L > kRing ? (L - kRecent + kPage - 1) / kPage : 0;
   return ring_units(mode, L) + 4 * pages;
 }
-// Planning cost, in eighths of a packed step (16 tokens), as measured on
-// GB300: a packed or BF16-page step costs 8; a ring step 19 (its BF16 tile
-// runs 16 tokens per barrier pair, packed pages 64: 3300 against 1370
-// cycles per 16 tokens); the first ring unit of a sequence carries kItemCost
-// more for the item switch (query load, epilogue) of the CTA that starts it.
-constexpr int kCostStep = 8, kCostRing = 19, kItemCost = 40;
-__device__ __forceinline__ int ring_cost(int R) { return R > 0 ? kItemCost + kCostRing * R : 0; }
-static_assert(4 * kCostStep <= kPlanCostPerPage && kItemCost + kCostRing * kRingChunks <= kPlanCostRingMax,
+// Planning cost (DecodeParams cost_*), by default in eighths of a packed
+// step (16 tokens) as measured on GB300: a packed or BF16-page step costs 8;
+// a ring step 19 (its BF16 tile runs 16 tokens per barrier pair, packed
+// pages 64: 3300 against 1370 cycles per 16 tokens); the first ring unit of a
+// sequence carries 40 more for the item switch (query load, epilogue) of the
+// CTA that starts it. The host keeps 4 * step <= kPlanCostPerPage and
+// item + 9 * ring <= kPlanCostRingMax, the bounds of its overflow check.
+static_assert(4 * kDefCostStep <= kPlanCostPerPage && kDefCostItem + kDefCostRing * kRingChunks <= kPlanCostRingMax,
               "planner cost bounds");
-__device__ __forceinline__ int seq_cost(int mode, int L) {
+__device__ __forceinline__ int ring_cost(const DecodeParams& p, int R) {
+  return R > 0 ? p.cost_item + p.cost_ring * R : 0;
+}
+__device__ __forceinline__ int seq_cost(const DecodeParams& p, int mode, int L) {
   const int R = ring_units(mode, L);
-  return ring_cost(R) + kCostStep * (seq_units(mode, L) - R);
+  return ring_cost(p, R) + p.cost_step * (seq_units(mode, L) - R);
 }
 // Unit index of a cost offset inside a sequence that lies on a unit boundary.
-__device__ __forceinline__ int cost_to_unit(int mode, int L, int x) {
+__device__ __forceinline__ int cost_to_unit(const DecodeParams& p, int mode, int L, int x) {
   const int R = ring_units(mode, L);
-  const int xr = ring_cost(R);
-  if (x >= xr) return R + (x - xr) / kCostStep;
-  return x < kItemCost + kCostRing ? 0 : (x - kItemCost) / kCostRing;
+  const int xr = ring_cost(p, R);
+  if (x >= xr) return R + (x - xr) / p.cost_step;
+  return x < p.cost_item + p.cost_ring ? 0 : (x - p.cost_item) / p.cost_ring;
 }
 
 // ---------------------------------------------------------------------------
@@ -224,7 +228,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, in
       const int Lraw = p.seq_lens[b];
       if (Lraw > p.max_tokens) atomicOr(p.status, MLAQ_DEV_SEQ_OVERFLOW);
       const int L = clamp_len(Lraw, p.max_tokens);
-      u = seq_cost(mode, L);
+      u = seq_cost(p, mode, L);
       if (L == 0) {
         for (int k = 0; k < p.H * kDL; ++k) p.out[(size_t)b * p.H * kDL + k] = 0;
         for (int h = 0; h < p.H; ++h) p.lse[(size_t)b * p.H + h] = -INFINITY;
@@ -249,13 +253,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, in
     if (raw < U) {
       const int b = last_le(useq, 0, B, raw);
       const int R = ring_units(mode, clamp_len(p.seq_lens[b], p.max_tokens));
-      const int xr = ring_cost(R);
+      const int xr = ring_cost(p, R);
       int x = raw - useq[b];
+      const int cs = p.cost_step, cr = p.cost_ring, ci = p.cost_item;
       if (x < xr)
-        x = x < kItemCost + kCostRing ? 0 : kItemCost + ((x - kItemCost) / kCostRing) * kCostRing;
+        x = x < ci + cr ? 0 : ci + ((x - ci) / cr) * cr;
       else
-        x = xr + ((x - xr) / (mode == MLAQ_BF16 ? kCostStep : 4 * kCostStep)) *
-                     (mode == MLAQ_BF16 ? kCostStep : 4 * kCostStep);
+        x = xr + ((x - xr) / (mode == MLAQ_BF16 ? cs : 4 * cs)) * (mode == MLAQ_BF16 ? cs : 4 * cs);
       v = useq[b] + x;
     }
     bnd[c] = v;
@@ -316,7 +320,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, in
           const int u0 = useq[b], u1 = useq[b + 1];
           if (u1 == u0) continue;  // empty sequence: no item
           const int Lb = clamp_len(p.seq_lens[b], p.max_tokens);
-          const Item it{b, cost_to_unit(mode, Lb, max(bnd[c], u0) - u0), cost_to_unit(mode, Lb, min(bnd[c + 1], u1) - u0),
+          const Item it{b, cost_to_unit(p, mode, Lb, max(bnd[c], u0) - u0), cost_to_unit(p, mode, Lb, min(bnd[c + 1], u1) - u0),
                         c, Lb, 0, 0, 0};
           items[k] = it;
           if (k == v) {
@@ -1498,6 +1502,9 @@ cudaError_t launch_decode(mlaq_cache* c, const uint16_t* q_latent, const uint16_
   p.num_pages = c->num_pages;
   p.max_tokens = c->max_pages_per_seq * kPage;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.cost_step = c->cost_step;
+  p.cost_ring = c->cost_ring;
+  p.cost_item = c->cost_item;
 
   {
     // the planner's shared-memory arrays exceed 48 KB for large batches
@@ -1595,6 +1602,9 @@ int launch_decode_static(int mode, const void* codes, const void* meta, const vo
   c.workspace_bytes = kStaticScratchBytes;
   c.num_sms = g_static_sms[dev];
   c.decode_ctas = MLAQ_CTAS_PER_SM * c.num_sms < kMaxPlanCtas ? MLAQ_CTAS_PER_SM * c.num_sms : kMaxPlanCtas;
+  c.cost_step = kDefCostStep;
+  c.cost_ring = kDefCostRing;
+  c.cost_item = kDefCostItem;
   char* ws = static_cast<char*>(c.workspace);
   // the status word is sticky: start each call from zero
   if (cudaMemsetAsync(ws + kWsStatus, 0, sizeof(int), s) != cudaSuccess) return MLAQ_ERR_CUDA;

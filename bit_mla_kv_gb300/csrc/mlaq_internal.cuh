@@ -57,7 +57,9 @@ struct __align__(16) Item {
 
 // Upper bounds of the planner's per-sequence cost (32-bit prefix sums): per
 // page of a sequence, and for its ring plus item overhead.
-constexpr int kPlanCostPerPage = 32, kPlanCostRingMax = 224;
+constexpr int kPlanCostPerPage = 32, kPlanCostRingMax = 512;
+// Default planning costs (see the planner): packed step, ring step, item start.
+constexpr int kDefCostStep = 8, kDefCostRing = 19, kDefCostItem = 40;
 inline bool plan_cost_fits(int max_seqs, int max_pages_per_seq) {
   return (long long)max_seqs * ((long long)max_pages_per_seq * kPlanCostPerPage + kPlanCostRingMax) < 0x7fffffffLL;
 }
@@ -318,6 +320,7 @@ struct mlaq_cache {
   size_t workspace_bytes;
   int num_sms;
   int decode_ctas;
+  int cost_step, cost_ring, cost_item;  // planner costs (mlaq_set_plan_costs)
   // timing
   int timing_max;
   int timing_n;

@@ -33,7 +33,7 @@ _szp = ctypes.POINTER(ctypes.c_size_t)
 EXPORTED = [
     "mlaq_buffer_sizes", "mlaq_cache_create", "mlaq_cache_destroy", "mlaq_append", "mlaq_decode",
     "mlaq_export_tokens", "mlaq_cache_bytes", "mlaq_get_device_status", "mlaq_clear_device_status",
-    "mlaq_timing_enable", "mlaq_timing_read", "mlaq_set_decode_ctas", "mlaq_status_string",
+    "mlaq_timing_enable", "mlaq_timing_read", "mlaq_set_decode_ctas", "mlaq_set_plan_costs", "mlaq_status_string",
     "mlaq_decode_noalloc", "mlaq_debug_wait_probe", "mlaq_decode_mtp",
 ]
 
@@ -52,6 +52,7 @@ _lib.mlaq_clear_device_status.argtypes = [_vp, _vp]
 _lib.mlaq_timing_enable.argtypes = [_vp, _i32]
 _lib.mlaq_timing_read.argtypes = [_vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(_i32)]
 _lib.mlaq_set_decode_ctas.argtypes = [_vp, _i32]
+_lib.mlaq_set_plan_costs.argtypes = [_vp, _i32, _i32, _i32]
 _lib.mlaq_decode_noalloc.argtypes = [ctypes.c_int, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _i32,
                                      ctypes.c_float, _vp, _vp, _vp, _vp]
 _lib.mlaq_debug_wait_probe.argtypes = [_vp, _i32, _i32, _vp]
@@ -281,3 +282,6 @@ class Cache:
 
     def set_decode_ctas(self, ctas: int):
         _check(_lib.mlaq_set_decode_ctas(self._h, ctas), "mlaq_set_decode_ctas")
+
+    def set_plan_costs(self, step: int, ring: int, item: int):
+        _check(_lib.mlaq_set_plan_costs(self._h, step, ring, item), "mlaq_set_plan_costs")

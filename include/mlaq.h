@@ -242,6 +242,15 @@ int mlaq_timing_read(mlaq_cache* cache, float* ms_out, int32_t* n);
 /* Number of CTAs the decode planner aims to fill (default 2 per SM). */
 int mlaq_set_decode_ctas(mlaq_cache* cache, int32_t ctas);
 
+/* Costs the decode planner balances across CTAs (a tuning knob; the results
+ * do not depend on it): `step` per 16-token step of a packed page or BF16
+ * page, `ring` per 16-slot chunk of the BF16 sink/recent ring, `item` once per
+ * sequence for the CTA that starts it. Defaults 8, 19, 40 (measured on
+ * GB300). Requires 1 <= step <= 8, ring >= 1, item >= 0 and
+ * item + 9 * ring <= 512, else MLAQ_ERR_SHAPE and the costs are unchanged.
+ * Host call; takes effect at the next decode. */
+int mlaq_set_plan_costs(mlaq_cache* cache, int32_t step, int32_t ring, int32_t item);
+
 /* Test hook for the bounded waits behind MLAQ_DEV_TIMEOUT (the decode kernel
  * waits on mbarriers for its bulk copies and its tensor-core MMAs, each wait
  * limited in wall time, never a trap). Launches one CTA of 32 threads that

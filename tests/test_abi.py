@@ -62,7 +62,7 @@ def test_host_argument_errors(lib):
     assert lib.mlaq_cache_create(ctypes.byref(out), 7, 1, 1, 1, 16, None, None, None, None, ctypes.c_size_t(0)) == -2
     assert lib.mlaq_cache_create(ctypes.byref(out), 0, 0, 1, 1, 16, None, None, None, None, ctypes.c_size_t(0)) == -3
     assert lib.mlaq_cache_create(ctypes.byref(out), 0, 1, 1, 1, 16, None, None, None, None, ctypes.c_size_t(0)) == -1
-    # plan cost sums would overflow 32 bits: 16384 * (32 * 5000 + 224) >= 2^31
+    # plan cost sums would overflow 32 bits: 16384 * (32 * 5000 + 512) >= 2^31
     assert lib.mlaq_cache_create(ctypes.byref(out), 0, 1, 16384, 5000, 16, None, None, None, None, ctypes.c_size_t(0)) == -3
     buf = ctypes.create_string_buffer(64)
     addr = (ctypes.addressof(buf) + 15) // 16 * 16
@@ -71,6 +71,7 @@ def test_host_argument_errors(lib):
     assert lib.mlaq_decode(None, None, None, None, None, 1, 16, ctypes.c_float(1.0), None, None, None) == -1
     assert lib.mlaq_append(None, None, None, 1, None, None, 1, None, 0, None) == -1
     assert lib.mlaq_timing_enable(None, 4) == -1
+    assert lib.mlaq_set_plan_costs(None, 8, 19, 40) == -1
     # multi-token decode: Q * H <= 128, H a multiple of 16
     assert lib.mlaq_decode_mtp(None, None, None, None, None, 1, 2, 16, ctypes.c_float(1.0), None, None, None) == -1
     # the bounded-wait test hook checks its arguments before any launch

@@ -276,6 +276,24 @@ def test_decode_running_max_rescale(mode):
             assert_close_out(out[b], lse[b], ro, rl, f"{mode} ctas={ctas} seq {b}")
 
 
+@pytest.mark.parametrize("costs", [(8, 19, 40), (1, 50, 0), (8, 1, 500), (3, 7, 100)])
+def test_plan_costs_change_only_the_split(costs):
+    # The planner's costs move the CTA boundaries (and so the split points and
+    # the combine), never the result; out-of-range costs are refused.
+    case = Case("C4R4", [700, 1500, 3000, 133, 65], 16, seed=21)
+    case.build()
+    from bit_mla_kv_gb300.mlaq import MlaqError
+    with pytest.raises(MlaqError):
+        case.cache.set_plan_costs(9, 19, 40)   # 4 * step > 32
+    with pytest.raises(MlaqError):
+        case.cache.set_plan_costs(8, 60, 0)    # item + 9 * ring > 512
+    case.cache.set_plan_costs(*costs)
+    out, lse = case.decode()
+    for b in range(case.B):
+        ro, rl = case.oracle_seq(b)
+        assert_close_out(out[b], lse[b], ro, rl, f"costs {costs} seq {b}")
+
+
 def test_split_invariance():
     case = Case("C4R4", [3000, 9000, 133, 640], 16, seed=15)
     case.build()
