@@ -119,7 +119,13 @@ class ClockSampler:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
                  "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            # the tool's start-up (driver queries) must not overlap the timed
+            # steps: wait until its first sample is written (at most 5 s)
+            t_end = time.time() + 5.0
             time.sleep(0.3)
+            while time.time() < t_end and os.path.getsize(self.path) == 0 and self.proc.poll() is None:
+                time.sleep(0.05)
+            time.sleep(0.15)
         except Exception:
             self.proc = None
 
@@ -282,6 +288,11 @@ def run_mlaq(args, ws, rank, local):
         cache.append(inp["pt"], seq, inp["cn"][i], inp["kn"][i])
         cache.decode(inp["ql"], inp["qr"], inp["pt"], seq, W.SOFTMAX_SCALE, out=out, lse=lse)
 
+    # The clock sampler starts before the warm-up, so that neither its
+    # start-up nor an idle GPU sits right before the timed steps.
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
     for i in range(Wm):
         l2_flush()
         step(i)
@@ -289,9 +300,6 @@ def run_mlaq(args, ws, rank, local):
     lens_at_start = [int(x) for x in seq.cpu().tolist()]
     # Timed steps: events only at step boundaries, so the append -> plan ->
     # decode -> combine chain keeps its programmatic-launch overlap.
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    sampler = ClockSampler(local)
-    sampler.start()
     barrier(ws)
     torch.cuda.synchronize()
     for j in range(K):
