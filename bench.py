@@ -400,6 +400,10 @@ def run_mlaq(args, ws, rank, local):
     ev_out = [torch.cuda.Event() for _ in range(K)]
     h2d = n_in
     d2h = n_res
+    # the host-side setup above leaves the GPU idle: a few decode calls (they
+    # read the cache and change nothing) keep it busy up to the timed steps
+    for _ in range(3):
+        cache.decode(inp["ql"], inp["qr"], inp["pt"], seq, W.SOFTMAX_SCALE, out=out, lse=lse)
     barrier(ws)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
