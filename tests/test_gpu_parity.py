@@ -385,11 +385,14 @@ def test_bounded_wait_runs_out_and_reports_status():
     assert case.cache.device_status() == 0
 
 
-@pytest.mark.parametrize("name,sample", [("v2lite_c4r4", [0, 7, 19, 31]), ("v3_c4r4", [0, 63]),
+@pytest.mark.parametrize("name,sample", [("v2lite_c4r4", [0, 7, 19, 31]), ("v2lite_c2r4", [3, 30]),
+                                         ("v2lite_bf16", [5]), ("v3_c4r4", [0, 63]),
                                          ("long_c2r4", [2]), ("long_c4r4", [1]), ("long_bf16", [3])])
 def test_full_size_sampled(name, sample):
-    """Full workload sizes in the benchmark's launch configuration; the oracle
-    checks whole sampled sequences."""
+    """Full workload sizes in the benchmark's launch configuration (the whole
+    workload through the bulk writer in one varlen call, then one decode); the
+    oracle checks whole sampled sequences: every code and meta word bit for
+    bit, and the decode output."""
     wl = W.workload(name)
     case = Case(wl.mode, wl.seq_lens, wl.H, seed=wl.seed, gen_device="cuda")
     case.build()
@@ -399,6 +402,16 @@ def test_full_size_sampled(name, sample):
     for b in sample:
         ro, rl = case.oracle_seq(b)
         assert_close_out(out[b], lse[b], ro, rl, f"{name} seq {b}")
+        if wl.mode == "BF16":
+            continue
+        L = case.seq_lens[b]
+        tb = torch.full((L,), b, dtype=torch.int32, device="cuda")
+        tt = torch.arange(L, dtype=torch.int32, device="cuda")
+        codes, meta = case.cache.export_tokens(case.pt_d, tb, tt)
+        ec, em = expected_codes(case, b)
+        np.testing.assert_array_equal(codes.cpu().numpy(), ec, err_msg=f"{name} codes seq {b}")
+        np.testing.assert_array_equal(meta.cpu().numpy().view(np.uint16), em.view(np.uint16),
+                                      err_msg=f"{name} meta seq {b}")
 
 
 @pytest.mark.parametrize("mode", ["C4R4", "BF16"])
