@@ -243,36 +243,7 @@ def build_inputs(wl, rank, device, total_steps):
     return dict(c=c, k=k, cu=cu, ql=ql, qr=qr, cn=cn, kn=kn, pt=pt.to(device), num_pages=num_pages, seed=seed)
 
 
-def run_mlaq(args, ws, rank, local):
-    from bit_mla_kv_gb300 import build as B
-    B.build()
-    from bit_mla_kv_gb300.mlaq import Cache
-
-    device = torch.device("cuda", local)
-    torch.cuda.set_device(device)
-    wl = W.workload(args.workload)
-    K, Wm = args.steps, args.warmup
-    inp = build_inputs(wl, rank, device, Wm + 3 * K)  # warmup + timed + instrumented + e2e steps
-    cache = Cache(wl.mode, inp["num_pages"], wl.B, inp["pt"].shape[1], max_heads=max(wl.H, 16), device=device)
-    seq = torch.zeros(wl.B, dtype=torch.int32, device=device)
-    cu_d = inp["cu"].to(device)
-    # prefill: the whole workload through the fused writer in one varlen call
-    # (inputs far larger than L2); the second of two identical calls (same
-    # tokens at the same positions, the same bytes written) is timed
-    cache.append(inp["pt"], seq, inp["c"], inp["k"], cu_new=cu_d)
-    seq.zero_()
-    torch.cuda.synchronize()
-    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    p0.record()
-    cache.append(inp["pt"], seq, inp["c"], inp["k"], cu_new=cu_d)
-    p1.record()
-    torch.cuda.synchronize()
-    assert cache.device_status() == 0, "writer reported a device error"
-    prefill_ms = p0.elapsed_time(p1)
-    ntok = int(sum(wl.seq_lens))
-    pf_bytes = prefill_bytes(wl.seq_lens, wl.mode)
-    out = torch.empty(wl.B, wl.H, 512, dtype=torch.bfloat16, device=device)
-    lse = torch.empty(wl.B, wl.H, dtype=torch.float32, device=device)
+def make_l2_flush(device):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     clean = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     sink = torch.empty(1, dtype=torch.float32, device=device)
@@ -283,80 +254,199 @@ def run_mlaq(args, ws, rank, local):
         # lines are written back here and not inside the timed decode.
         flush.zero_()
         torch.sum(clean, dim=0, keepdim=True, out=sink)
+    return l2_flush
 
-    def step(i):
-        cache.append(inp["pt"], seq, inp["cn"][i], inp["kn"][i])
-        cache.decode(inp["ql"], inp["qr"], inp["pt"], seq, W.SOFTMAX_SCALE, out=out, lse=lse)
 
-    # The clock sampler starts before the warm-up, so that neither its
-    # start-up nor an idle GPU sits right before the timed steps.
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    sampler = ClockSampler(local)
-    sampler.start()
+class Workbench:
+    """One workload on one device: its seeded inputs, a cache filled by the
+    fused writer, and the step (append one token per sequence + decode)."""
+
+    def __init__(self, wl, rank, device, total_steps):
+        from bit_mla_kv_gb300.mlaq import Cache
+        self.wl, self.device = wl, device
+        self.inp = build_inputs(wl, rank, device, total_steps)
+        self.cache = Cache(wl.mode, self.inp["num_pages"], wl.B, self.inp["pt"].shape[1], max_heads=max(wl.H, 16),
+                           device=device)
+        self.seq = torch.zeros(wl.B, dtype=torch.int32, device=device)
+        self.cu_d = self.inp["cu"].to(device)
+        self.out = torch.empty(wl.B, wl.H, 512, dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty(wl.B, wl.H, dtype=torch.float32, device=device)
+
+    def prefill(self):
+        """The whole workload through the fused writer in one varlen call
+        (inputs far larger than L2); the second of two identical calls (same
+        tokens at the same positions, the same bytes written) is timed."""
+        inp = self.inp
+        self.cache.append(inp["pt"], self.seq, inp["c"], inp["k"], cu_new=self.cu_d)
+        self.seq.zero_()
+        torch.cuda.synchronize()
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record()
+        self.cache.append(inp["pt"], self.seq, inp["c"], inp["k"], cu_new=self.cu_d)
+        p1.record()
+        torch.cuda.synchronize()
+        assert self.cache.device_status() == 0, "writer reported a device error"
+        ms = p0.elapsed_time(p1)
+        pf = prefill_bytes(self.wl.seq_lens, self.wl.mode)
+        return {"tokens": int(sum(self.wl.seq_lens)), "us": ms * 1e3, "bytes": pf, "GB/s": pf / (ms * 1e-3) / 1e9,
+                "how": "varlen mlaq_append of every sequence in one call (the second of two identical calls), "
+                       "CUDA events"}
+
+    def append(self, i):
+        self.cache.append(self.inp["pt"], self.seq, self.inp["cn"][i], self.inp["kn"][i])
+
+    def decode(self):
+        self.cache.decode(self.inp["ql"], self.inp["qr"], self.inp["pt"], self.seq, W.SOFTMAX_SCALE, out=self.out,
+                          lse=self.lse)
+
+    def step(self, i):
+        self.append(i)
+        self.decode()
+
+    def lens(self):
+        return [int(x) for x in self.seq.cpu().tolist()]
+
+    def release(self):
+        for name in ("inp", "cache", "seq", "cu_d", "out", "lse"):
+            setattr(self, name, None)
+        torch.cuda.empty_cache()
+
+
+def roofline_for(wl, mean_lens, kern_ms):
+    """Roofline of one mlaq_decode call (plan + decode + combine) for the
+    workload at the given (mean) sequence lengths."""
+    dec_bytes = decode_bytes(mean_lens, wl.mode, wl.B, wl.H)
+    hbm, tf_burst, tf_sus, peak_src = load_peaks()
+    flops = decode_flops(mean_lens, wl.H)
+    t_mem = dec_bytes / (hbm * 1e9)
+    t_ten = flops / (tf_burst * 1e12)
+    if t_mem >= t_ten:
+        achieved = dec_bytes / (kern_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "peak_source": f"{peak_src} hbm_gbs (copy)"}
+    else:
+        achieved = flops / (kern_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tf_burst, "unit": "TFLOP/s",
+                "frac": achieved / tf_burst, "peak_source": f"{peak_src} bf16_tflops (burst)"}
+    roof["kernel_ms"] = kern_ms
+    roof["roofline_us"] = max(t_mem, t_ten) * 1e6
+    roof["algorithmic_bytes"] = dec_bytes
+    roof["algorithmic_flops"] = flops
+    return roof
+
+
+def measure_steps(wb, K, Wm, l2_flush, ws, device, first_step=0):
+    """Wm warm-up steps, K timed steps (events at step boundaries only, L2
+    flushed between steps outside the events), then K instrumented steps
+    (an event after the append, the library's events around mlaq_decode)."""
     for i in range(Wm):
         l2_flush()
-        step(i)
+        wb.step(first_step + i)
     torch.cuda.synchronize()
-    lens_at_start = [int(x) for x in seq.cpu().tolist()]
-    # Timed steps: events only at step boundaries, so the append -> plan ->
-    # decode -> combine chain keeps its programmatic-launch overlap.
+    lens_at_start = wb.lens()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     barrier(ws)
     torch.cuda.synchronize()
     for j in range(K):
         l2_flush()
         evs[j][0].record()
-        step(Wm + j)
+        wb.step(first_step + Wm + j)
         evs[j][1].record()
     torch.cuda.synchronize()
     barrier(ws)
-    clocks = sampler.stop()
-    step_ms = [a.elapsed_time(b) for a, b in evs]
-    ms = sum(step_ms) / K
+    ms = sum(a.elapsed_time(b) for a, b in evs) / K
     ms_max = max_over_ranks(ms, ws, device)
+    wl = wb.wl
     mean_lens = [L + (K - 1) / 2.0 for L in lens_at_start]
     bytes_step = decode_bytes(mean_lens, wl.mode, wl.B, wl.H) + append_bytes(wl.B, wl.mode)
     bytes_all = sum_over_ranks(bytes_step, ws, device)
-    value = bytes_all / (ms_max * 1e-3) / 1e9
-    # Instrumented steps (the next K): the library's events around each
-    # mlaq_decode call (plan + decode + combine) and an event after the append.
-    lens_inst = [int(x) for x in seq.cpu().tolist()]
-    cache.timing_enable(K)
+    lens_inst = wb.lens()
+    wb.cache.timing_enable(K)
     ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     mid = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     torch.cuda.synchronize()
     for j in range(K):
         l2_flush()
         ev2[j][0].record()
-        cache.append(inp["pt"], seq, inp["cn"][Wm + K + j], inp["kn"][Wm + K + j])
+        wb.append(first_step + Wm + K + j)
         mid[j].record()
-        cache.decode(inp["ql"], inp["qr"], inp["pt"], seq, W.SOFTMAX_SCALE, out=out, lse=lse)
+        wb.decode()
         ev2[j][1].record()
     torch.cuda.synchronize()
     append_ms = sum(a.elapsed_time(m) for (a, _), m in zip(ev2, mid)) / K
     inst_step_ms = sum(a.elapsed_time(b) for a, b in ev2) / K
-    kern_ms = cache.timing_read()
-    cache.timing_enable(0)
+    kern_ms = wb.cache.timing_read()
+    wb.cache.timing_enable(0)
     kern_avg = sum(kern_ms) / max(len(kern_ms), 1)
-    mean_inst = [L + (K - 1) / 2.0 for L in lens_inst]
-    dec_bytes = decode_bytes(mean_inst, wl.mode, wl.B, wl.H)
-    hbm, tf_burst, tf_sus, peak_src = load_peaks()
-    flops = decode_flops(mean_inst, wl.H)
-    t_mem = dec_bytes / (hbm * 1e9)
-    t_ten = flops / (tf_burst * 1e12)
-    bound = "hbm" if t_mem >= t_ten else "tensor"
-    if bound == "hbm":
-        achieved = dec_bytes / (kern_avg * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "peak_source": f"{peak_src} hbm_gbs (copy)"}
-    else:
-        achieved = flops / (kern_avg * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": tf_burst, "unit": "TFLOP/s",
-                "frac": achieved / tf_burst, "peak_source": f"{peak_src} bf16_tflops (burst)"}
+    roof = roofline_for(wl, [L + (K - 1) / 2.0 for L in lens_inst], kern_avg)
+    assert wb.cache.device_status() == 0, "device error during the benchmark"
+    return {"ms_max": ms_max, "bytes_all": bytes_all, "value": bytes_all / (ms_max * 1e-3) / 1e9,
+            "lens_at_start": lens_at_start, "append_ms": append_ms, "inst_step_ms": inst_step_ms,
+            "kern_avg": kern_avg, "roof": roof}
+
+
+PER_CONFIG_DEFAULT = "v2lite_c2r4,v2lite_bf16,v3_c4r4,long_c2r4,long_c4r4,long_bf16,serving_c4r4"
+
+
+def run_per_config(names, K, Wm, l2_flush, ws, rank, device, local):
+    """The other workloads, each with its own cache, K timed steps and its own
+    clock record; one line of numbers per workload."""
+    res = {}
+    for name in names:
+        wl = W.workload(name)
+        wb = Workbench(wl, rank, device, Wm + 2 * K)
+        pre = wb.prefill()
+        sampler = ClockSampler(local)
+        sampler.start()
+        m = measure_steps(wb, K, Wm, l2_flush, ws, device)
+        clocks = sampler.stop()
+        roof = m["roof"]
+        res[name] = {"workload": wl.description, "steps": K, "warmup": Wm,
+                     "step_us": m["ms_max"] * 1e3, "GB/s": m["value"],
+                     "decode_call_us": m["kern_avg"] * 1e3, "append_us": m["append_ms"] * 1e3,
+                     "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac", "roofline_us")},
+                     "writer_prefill_GB/s": pre["GB/s"], "clocks": clocks}
+        wb.release()
+    return res
+
+
+def compression_record(cache, mode, seq_lens):
+    """Persistent-cache accounting through the library (mlaq_cache_bytes):
+    policy bytes vs the same sequences in a paged all-BF16 cache."""
+    rec = {"how": "mlaq_cache_bytes: BF16 sink/recent ring + packed copies of all tokens + page mapping, "
+                  "against a paged all-BF16 cache (onedev.kr system-efficiency paragraph)", "mode": mode}
+    for label, lens in (("workload", seq_lens), ("4K", [4096]), ("128K", [131072])):
+        pol, ref = cache.cache_bytes(lens)
+        rec[label] = {"policy_bytes": pol, "bf16_bytes": ref, "ratio": ref / pol}
+    rec["pages_quote"] = {"4K": 3.22, "128K": 3.59}
+    return rec
+
+
+def run_mlaq(args, ws, rank, local):
+    from bit_mla_kv_gb300 import build as B
+    B.build()
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    wl = W.workload(args.workload)
+    K, Wm = args.steps, args.warmup
+    wb = Workbench(wl, rank, device, Wm + 3 * K)  # warmup + timed + instrumented + e2e steps
+    prefill = wb.prefill()
+    l2_flush = make_l2_flush(device)
+    inp, cache, seq, out, lse = wb.inp, wb.cache, wb.seq, wb.out, wb.lse
+
+    # The clock sampler starts before the warm-up, so that neither its
+    # start-up nor an idle GPU sits right before the timed steps.
+    sampler = ClockSampler(local)
+    sampler.start()
+    m = measure_steps(wb, K, Wm, l2_flush, ws, device)
+    clocks = sampler.stop()
+    ms_max, bytes_all, value = m["ms_max"], m["bytes_all"], m["value"]
+    lens_at_start, kern_avg = m["lens_at_start"], m["kern_avg"]
+    roof = dict(m["roof"])
     roof["traffic"] = recorded_traffic(args.workload)
     roof["kernel"] = "mlaq_decode: plan_kernel + decode_kernel (split-KV attention) + combine_kernel"
-    roof["kernel_ms"] = kern_avg
-    roof["roofline_us"] = max(t_mem, t_ten) * 1e6
-    roof["frac_of_roofline_kernel"] = max(t_mem, t_ten) * 1e3 / kern_avg
+    roof["frac_of_roofline_kernel"] = roof["roofline_us"] * 1e-3 / kern_avg
 
     # ---- end to end through the public API with host buffers
     # A step's inputs (queries and the new token of every sequence) travel in
@@ -403,7 +493,7 @@ def run_mlaq(args, ws, rank, local):
     # the host-side setup above leaves the GPU idle: a few decode calls (they
     # read the cache and change nothing) keep it busy up to the timed steps
     for _ in range(3):
-        cache.decode(inp["ql"], inp["qr"], inp["pt"], seq, W.SOFTMAX_SCALE, out=out, lse=lse)
+        wb.decode()
     barrier(ws)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -433,6 +523,14 @@ def run_mlaq(args, ws, rank, local):
     e2e_s = max_over_ranks(e2e_s, ws, device)
     e2e_val = bytes_all / e2e_s / 1e9
     assert cache.device_status() == 0, "device error during the benchmark"
+    compression = compression_record(cache, wl.mode, wl.seq_lens)
+    wb.release()
+    del d_in, d_res, v_ql, v_qr, v_cn, v_kn, v_out, v_lse
+
+    per_config = None
+    names = [n for n in args.per_config.split(",") if n and n != "none" and n != args.workload]
+    if names:
+        per_config = run_per_config(names, args.per_config_steps, 3, l2_flush, ws, rank, device, local)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -465,13 +563,13 @@ def run_mlaq(args, ws, rank, local):
                        "out/lse back into one pinned buffer; copies on their own streams into double buffers, "
                        "ordered by events, overlap the neighbouring steps' kernels; one synchronize at the end"},
         "gpu_launches": 4 * K,  # per step: append, plan, decode, combine
-        "step_breakdown": {"append_us": append_ms * 1e3, "decode_call_us": kern_avg * 1e3,
-                           "step_us": inst_step_ms * 1e3,
+        "step_breakdown": {"append_us": m["append_ms"] * 1e3, "decode_call_us": kern_avg * 1e3,
+                           "step_us": m["inst_step_ms"] * 1e3,
                            "how": "K more steps with an event after the append and the library's events "
                                   "around mlaq_decode (these break the launch overlap the timed steps keep)"},
-        "writer_prefill": {"tokens": ntok, "us": prefill_ms * 1e3, "bytes": pf_bytes,
-                           "GB/s": pf_bytes / (prefill_ms * 1e-3) / 1e9,
-                           "how": "varlen mlaq_append of every sequence in one call (the second of two identical calls), CUDA events"},
+        "writer_prefill": prefill,
+        "compression": compression,
+        "per_config": per_config,
         "clocks": clocks,
         "impl": "mlaq",
     }
@@ -533,6 +631,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=2.0, help="seconds of oracle work per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--per-config", default=PER_CONFIG_DEFAULT,
+                    help="comma-separated other workloads measured after the headline ('none' to skip)")
+    ap.add_argument("--per-config-steps", type=int, default=10)
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

@@ -40,6 +40,9 @@
 //    (s, mn) = (1, 0).
 #include <math.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "mlaq_internal.cuh"
 
 namespace mlaq {
@@ -570,10 +573,19 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
   // Query fragments (B operand of the score MMA: k = channel, n = head) of
   // heads h0 + hoff .. h0 + hoff + 15, with the per-group query sums of the
   // min-term MMA.
+  // A query element beyond +-65504 (or NaN), or a per-group query sum whose
+  // fp16 split overflows, sets MLAQ_DEV_RANGE (the sequence's output is then
+  // undefined; the other sequences are unaffected).
   auto make_q_frags = [&](int b, int hoff, uint32_t (&QF)[2][4][2][2], uint32_t (&QR)[2][2], uint32_t (&KM)[2]) {
     float k2[3][2];
     const uint16_t* ql = p.q_latent + ((size_t)b * H + h0) * kDL;
     const uint16_t* qp = p.q_rope + ((size_t)b * H + h0) * kDR;
+    bool qbad = false;
+    auto ld_q = [&](const uint16_t* src) {
+      const uint32_t u = *reinterpret_cast<const uint32_t*>(src);
+      qbad |= (u & 0x7fffu) > 0x477fu || ((u >> 16) & 0x7fffu) > 0x477fu;
+      return bf2_to_h2(u);
+    };
 #pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
       const int h = hoff + 8 * hb + r;
@@ -583,8 +595,8 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const int c = 64 * (2 * w + j) + 16 * kk + 2 * i;
-          QF[j][kk][hb][0] = bf2_to_h2(*reinterpret_cast<const uint32_t*>(ql + (size_t)h * kDL + c));
-          QF[j][kk][hb][1] = bf2_to_h2(*reinterpret_cast<const uint32_t*>(ql + (size_t)h * kDL + c + 8));
+          QF[j][kk][hb][0] = ld_q(ql + (size_t)h * kDL + c);
+          QF[j][kk][hb][1] = ld_q(ql + (size_t)h * kDL + c + 8);
           const float2 a = __half22float2(u32_as_h2(QF[j][kk][hb][0]));
           const float2 bq = __half22float2(u32_as_h2(QF[j][kk][hb][1]));
           acc += (a.x + a.y) + (bq.x + bq.y);
@@ -592,8 +604,8 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
         k2[j][hb] = acc;
       }
       const int c = 16 * w + 2 * i;
-      QR[hb][0] = bf2_to_h2(*reinterpret_cast<const uint32_t*>(qp + (size_t)h * kDR + c));
-      QR[hb][1] = bf2_to_h2(*reinterpret_cast<const uint32_t*>(qp + (size_t)h * kDR + c + 8));
+      QR[hb][0] = ld_q(qp + (size_t)h * kDR + c);
+      QR[hb][1] = ld_q(qp + (size_t)h * kDR + c + 8);
       const float2 a = __half22float2(u32_as_h2(QR[hb][0]));
       const float2 bq = __half22float2(u32_as_h2(QR[hb][1]));
       k2[2][hb] = (a.x + a.y) + (bq.x + bq.y);
@@ -611,10 +623,12 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
 #pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
       const float v = (i == 0) ? k2[0][hb] : (i == 1) ? k2[1][hb] : k2[2][hb];
+      qbad |= !(fabsf(v) < 65520.f);
       const __half hi = __float2half_rn(v);
       const __half lo = __float2half_rn(v - __half2float(hi));
       KM[hb] = (i < 3) ? h2_as_u32(__halves2half2(hi, lo)) : 0u;
     }
+    if (__any_sync(0xffffffffu, qbad) && lane == 0) atomicOr(p.status, MLAQ_DEV_RANGE);
   };
   // The second half's fragments: 38 words per thread, as 10 uint4 rows
   // [row][thread] (each thread reads back only its own words).
@@ -1430,20 +1444,45 @@ static cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, si
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// Opt every decode-path kernel into its dynamic shared memory (> 48 KB), once
+// per device and for all variants together, so that the first decode call on
+// a device, whatever its mode and head count, is the only one that changes a
+// function attribute (it must run outside a stream capture). Serialised
+// across host threads.
+template <int MODE, int NH>
+static cudaError_t set_decode_attr() {
+  return cudaFuncSetAttribute(decode_kernel<MODE, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sizeof(DecodeSmem<NH>));
+}
+static cudaError_t set_all_decode_attrs() {
+  const cudaError_t es[] = {
+      set_decode_attr<MLAQ_C4R4, 16>(), set_decode_attr<MLAQ_C2R4, 16>(), set_decode_attr<MLAQ_BF16, 16>(),
+      set_decode_attr<MLAQ_C4R4, 32>(), set_decode_attr<MLAQ_C2R4, 32>(), set_decode_attr<MLAQ_BF16, 32>(),
+      // the planner's shared-memory arrays exceed 48 KB for large batches
+      cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)plan_smem_bytes(kMaxSeqs, kMaxPlanCtas))};
+  for (cudaError_t e : es)
+    if (e != cudaSuccess) return e;
+  return cudaSuccess;
+}
+static std::mutex g_attr_mutex;
+static std::atomic<bool> g_attr_done[kMaxDevices];
+cudaError_t decode_attrs_ready() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return set_all_decode_attrs();
+  if (g_attr_done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(g_attr_mutex);
+  if (g_attr_done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  e = set_all_decode_attrs();
+  if (e == cudaSuccess) g_attr_done[dev].store(true, std::memory_order_release);
+  return e;
+}
+
 template <int MODE, int NH>
 static cudaError_t run_decode(mlaq_cache* c, const DecodeParams& p, int grid_cta, cudaStream_t s) {
   const int smem = (int)sizeof(DecodeSmem<NH>);
-  // Opt in to >48 KB of dynamic shared memory once per device (the first call
-  // on a device must not be inside a stream capture).
-  static bool attr_done[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t ea = cudaGetDevice(&dev);
-  if (ea != cudaSuccess) return ea;
-  if (dev < 0 || dev >= kMaxDevices || !attr_done[dev]) {
-    ea = cudaFuncSetAttribute(decode_kernel<MODE, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (ea != cudaSuccess) return ea;
-    if (dev >= 0 && dev < kMaxDevices) attr_done[dev] = true;
-  }
   cudaEvent_t* ev = nullptr;
   if (c->timing_events && c->timing_n < c->timing_max)
     ev = reinterpret_cast<cudaEvent_t*>(c->timing_events) + 2 * c->timing_n;  // ev[0] precedes the plan
@@ -1472,9 +1511,8 @@ cudaError_t launch_decode(mlaq_cache* c, const uint16_t* q_latent, const uint16_
   // heads per CTA: 32 when H allows it (one unpack per page for both halves)
   const int NH = H % 32 == 0 ? 32 : 16;
   const int HB = H / NH;
-  // item slots (CTAs per head block); the planner's one-pass scan over CTA
-  // boundaries needs G + 1 <= 1024
-  const int G = max(1, min(kMaxPlanCtas - 1, c->decode_ctas / HB));
+  // item slots (CTAs per head block)
+  const int G = plan_slots(c->decode_ctas, HB, H);
 
   DecodeParams p;
   p.codes = static_cast<const uint8_t*>(c->codes);
@@ -1507,17 +1545,8 @@ cudaError_t launch_decode(mlaq_cache* c, const uint16_t* q_latent, const uint16_
   p.cost_item = c->cost_item;
 
   {
-    // the planner's shared-memory arrays exceed 48 KB for large batches
-    static bool plan_attr_done[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t ea = cudaGetDevice(&dev);
+    const cudaError_t ea = decode_attrs_ready();
     if (ea != cudaSuccess) return ea;
-    if (dev < 0 || dev >= kMaxDevices || !plan_attr_done[dev]) {
-      ea = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)plan_smem_bytes(kMaxSeqs, kMaxPlanCtas));
-      if (ea != cudaSuccess) return ea;
-      if (dev >= 0 && dev < kMaxDevices) plan_attr_done[dev] = true;
-    }
   }
   // timed (mlaq_timing_enable): plan + decode + combine
   if (c->timing_events && c->timing_n < c->timing_max)
@@ -1561,20 +1590,29 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 
 static void* g_static_ptr[kMaxDevices];
 static int g_static_sms[kMaxDevices];
+static std::atomic<bool> g_static_ready[kMaxDevices];
+static std::mutex g_static_mutex;
 
 // Once per device, with that device current: the scratch array's device
-// address (host code only sees a host-side stand-in for the symbol) and the
-// SM count the planner sizes the grid for.
+// address (host code only sees a host-side stand-in for the symbol), the SM
+// count the planner sizes the grid for, and every decode kernel variant's
+// attributes (so that no later call on this device changes one, whatever its
+// mode or head count). Serialised across host threads.
 static cudaError_t static_scratch_setup(int dev) {
-  if (g_static_ptr[dev]) return cudaSuccess;
+  if (g_static_ready[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(g_static_mutex);
+  if (g_static_ready[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  cudaError_t e = decode_attrs_ready();
+  if (e != cudaSuccess) return e;
   void* p = nullptr;
-  cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+  e = cudaGetSymbolAddress(&p, g_static_scratch);
   if (e != cudaSuccess) return e;
   int sms = 0;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   g_static_sms[dev] = sms;
   g_static_ptr[dev] = p;
+  g_static_ready[dev].store(true, std::memory_order_release);
   return cudaSuccess;
 }
 

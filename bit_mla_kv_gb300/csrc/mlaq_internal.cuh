@@ -37,6 +37,9 @@ constexpr size_t kWsAppendDone = 8;      // uint32 CTAs of the running append th
 constexpr int kMaxPlanCtas = 1024;       // decode CTA count never exceeds this
 constexpr int kMaxSeqs = 16384;          // sequences per call
 constexpr int kMaxHeadBlocks = 8;        // 128 heads / 16
+// Split partial rows the plan may add beyond one per (sequence, head): the
+// decode caps its item slots per head block at kPlanRowSlack / H.
+constexpr int kPlanRowSlack = 32 * kMaxPlanCtas;
 
 __host__ __device__ constexpr int content_bits(int mode) { return mode == MLAQ_C2R4 ? 2 : 4; }
 // Bytes of codes per token in a page (BF16 mode: the raw token).
@@ -66,9 +69,20 @@ inline bool plan_cost_fits(int max_seqs, int max_pages_per_seq) {
 
 // Items: at most one per sequence plus one per CTA boundary inside a sequence.
 inline size_t max_items_for(int max_seqs) { return (size_t)max_seqs + kMaxPlanCtas + 1; }
-// Rows (item, head) of the partial outputs: items * H <= B H + 16 * ctas.
+// Rows (item, head) of the partial outputs. A plan over G item slots has at
+// most B + G + 1 items, and G <= kPlanRowSlack / H, so items * H <= B H +
+// kPlanRowSlack + H.
 inline size_t max_partial_rows(int max_seqs, int max_heads) {
-  return (size_t)max_seqs * max_heads + (size_t)16 * kMaxPlanCtas + max_heads;
+  return (size_t)max_seqs * max_heads + (size_t)kPlanRowSlack + max_heads;
+}
+// Item slots (CTAs per head block) of a decode over H heads in HB head blocks
+// with `ctas` CTAs in all: the planner's one-pass scan over slot boundaries
+// needs G + 1 <= kMaxPlanCtas, and the partial rows need G * H <= kPlanRowSlack.
+inline int plan_slots(int ctas, int HB, int H) {
+  int G = ctas / HB;
+  if (G > kMaxPlanCtas - 1) G = kMaxPlanCtas - 1;
+  if (G > kPlanRowSlack / H) G = kPlanRowSlack / H;
+  return G < 1 ? 1 : G;
 }
 
 struct WsLayout {

@@ -73,7 +73,8 @@ typedef enum mlaq_status {
 #define MLAQ_DEV_SEQ_OVERFLOW 0x2 /* token position beyond max_pages_per_seq * 64 */
 #define MLAQ_DEV_NONFINITE 0x4    /* quantization metadata not finite in fp16 */
 #define MLAQ_DEV_TIMEOUT 0x8      /* a bounded wait on a bulk copy ran out */
-#define MLAQ_DEV_RANGE 0x10       /* a value outside the kernel's fp16 operand range */
+#define MLAQ_DEV_RANGE 0x10       /* a value outside the decode's fp16 operand range
+                                     (see mlaq_append and mlaq_decode) */
 
 #define MLAQ_PAGE_TOKENS 64
 #define MLAQ_SINK 4
@@ -133,6 +134,12 @@ int mlaq_cache_destroy(mlaq_cache* cache);
  * token 128 positions earlier, which from then on is read from its packed
  * copy (no re-quantization). In BF16 mode the BF16 token is stored in the
  * page instead. Invalid page entries set MLAQ_DEV_PAGE_OOB and skip the token.
+ * The decode computes on fp16 operands, so the writer checks their range: a
+ * BF16 copy (ring slot or BF16-mode page) holding a value beyond +-65504 or a
+ * NaN, or a packed group whose largest reconstructed value mn + (2^b - 1) * s
+ * reaches 65520, sets MLAQ_DEV_RANGE (non-finite metadata sets
+ * MLAQ_DEV_NONFINITE instead); the token is still stored, and decodes of its
+ * sequence are undefined while it is attended.
  */
 int mlaq_append(mlaq_cache* cache, const int32_t* page_table, int32_t* seq_lens, int32_t B,
                 const uint16_t* c_latent, const uint16_t* k_rope, int32_t n_new,
@@ -150,10 +157,15 @@ int mlaq_append(mlaq_cache* cache, const int32_t* page_table, int32_t* seq_lens,
  * kernel); all tokens share one softmax. L == 0 gives out = 0, lse = -inf.
  * Work is split over the GPU (split-KV) by a device-side planner from
  * seq_lens, and merged by a log-sum-exp combine kernel: three launches, no
- * host sync. Inputs must lie in fp16 range (|x| < 65504; the kernel computes
- * in fp16 operands with fp32 accumulation). The first call on a device opts
- * the attention kernel into large shared memory (a host-side attribute), so
- * make that first call outside any CUDA-graph capture; later calls capture.
+ * host sync. The kernel computes on fp16 operands with fp32 accumulation, so
+ * inputs must lie in fp16 range; this is checked: a query element beyond
+ * +-65504 or a NaN, or a per-group (64-channel) sum of one head's query
+ * beyond the fp16 range, sets MLAQ_DEV_RANGE (cached tokens are checked by
+ * the writer); that sequence's output is then undefined and the other
+ * sequences are unaffected. The first decode call on a device
+ * (any mode, any head count) opts every attention kernel variant into large
+ * shared memory (a host-side attribute), so make that first call outside any
+ * CUDA-graph capture; later calls capture.
  */
 int mlaq_decode(mlaq_cache* cache, const uint16_t* q_latent, const uint16_t* q_rope,
                 const int32_t* page_table, const int32_t* seq_lens, int32_t B, int32_t H,
@@ -192,11 +204,16 @@ int mlaq_decode_mtp(mlaq_cache* cache, const uint16_t* q_latent, const uint16_t*
  *   dev_status: optional device int32 that receives this call's device
  *       status bits (MLAQ_DEV_*), or NULL.
  * Calls nothing that allocates (no cudaMalloc / cudaFree, no allocating
- * library routine). Returns MLAQ_ERR_CAPACITY when the scratch needed for
- * (B, H) exceeds 64 MiB (about B * H <= 8192, e.g. B = 64 at H = 128 or
- * B = 512 at H = 16). The first call on each device looks up the array's
- * device address and sets a kernel attribute; make that first call before
- * any stream capture. Every call uses the same array and the next call
+ * library routine). The scratch needed for (B, H) is what mlaq_buffer_sizes
+ * reports as workspace_bytes for max_seqs = B, max_heads = H: about
+ * (B * H + 32768 + H) * 1028 bytes of split partials plus 36 * B + 38 KB of
+ * plan; when it exceeds 64 MiB the call returns MLAQ_ERR_CAPACITY and
+ * launches nothing. That admits B * H up to about 32,300: B <= 2022 at H = 16,
+ * 1011 at H = 32, 505 at H = 64, 252 at H = 128. The first call on each
+ * device looks up the array's device address and sets the shared-memory
+ * attribute of every decode kernel variant (all modes and head counts);
+ * make that first call before any stream capture. Every call uses the same
+ * array and the next call
  * overwrites it (the status word is cleared at the start of each call), so
  * calls that can overlap on the GPU -- on different streams, or on two
  * threads -- race and give wrong results; serialise them on one stream. */

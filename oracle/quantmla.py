@@ -53,7 +53,7 @@ __all__ = [
     "SINK", "RECENT", "GROUP", "D_LATENT", "D_ROPE", "D_QK", "N_GROUPS", "RING_SLOTS",
     "MODES", "mode_bits", "packed_bytes_per_token", "quantize_groups", "quantize_tokens",
     "pack_canonical", "unpack_canonical", "dequantize_tokens", "is_bf16_token",
-    "bf16_token_mask", "assemble_kv", "attend", "decode_sequence", "decode_batch",
+    "bf16_token_mask", "assemble_kv", "attend", "decode_sequence",
     "combine_partials", "expected_ring", "cache_bytes", "perturb_to_nmse", "path_response",
 ]
 
@@ -237,17 +237,6 @@ def decode_sequence(q_lat, q_rope, tokens_bf16, codes, meta, L, scale, mode, n_a
     return attend(q_lat, q_rope, kv, scale)
 
 
-def decode_batch(q_lat, q_rope, seqs, scale, mode):
-    """q_lat [B,H,512], q_rope [B,H,64]; seqs: list of (tokens_bf16 [L,576],
-    codes [L,576] or None, meta [L,9,2] or None, L). Returns out [B,H,512], lse [B,H]."""
-    B, H = q_lat.shape[:2]
-    out = np.zeros((B, H, D_LATENT))
-    lse = np.zeros((B, H))
-    for b, (tok, codes, meta, L) in enumerate(seqs):
-        out[b], lse[b] = decode_sequence(q_lat[b], q_rope[b], tok, codes, meta, L, scale, mode)
-    return out, lse
-
-
 def combine_partials(outs, lses):
     """Merge split partial results (each normalized over its own token range)
     into the single global softmax: lse = log sum_i exp(lse_i),
@@ -292,13 +281,17 @@ def cache_bytes(seq_lens, mode: str, page_tokens: int = 64, meta_bytes_per_token
                 page_entry_bytes: int = 4):
     """Persistent cache bytes under the mixed-precision policy, counted the way
     [ODK] 시스템 효율 paragraph counts them: BF16 buffers + packed copies of all
-    tokens + page mapping. Returns (packed_policy_bytes, bf16_cache_bytes)."""
-    packed_tok = packed_bytes_per_token(mode) + meta_bytes_per_token
+    tokens + page mapping. Returns (packed_policy_bytes, bf16_cache_bytes).
+    Mode 'BF16' is the paged all-BF16 cache the paragraph compares against, so
+    its policy bytes are its BF16 bytes (no ring, no packed copies)."""
+    bf16 = MODES[mode] is None
+    packed_tok = D_QK * 2 if bf16 else packed_bytes_per_token(mode) + meta_bytes_per_token
+    ring = 0 if bf16 else RING_SLOTS * D_QK * 2
     pol = 0
     ref = 0
     for L in seq_lens:
         pages = math.ceil(L / page_tokens)
-        pol += pages * page_tokens * packed_tok + RING_SLOTS * D_QK * 2 + pages * page_entry_bytes
+        pol += pages * page_tokens * packed_tok + ring + pages * page_entry_bytes
         ref += pages * page_tokens * D_QK * 2 + pages * page_entry_bytes
     return pol, ref
 

@@ -230,6 +230,130 @@ def test_decode_more_heads(mode, H):
             assert_close_out(out[b], lse[b], ro, rl, f"{mode} H={H} ctas={ctas} seq {b}")
 
 
+@pytest.mark.parametrize("mode,where", [("C4R4", "ring"), ("C4R4", "packed"), ("C2R4", "ring_small_append"),
+                                        ("BF16", "page")])
+def test_fp16_range_is_checked_for_tokens(mode, where):
+    # A cached value beyond the fp16 range (a ring copy, a packed-only token,
+    # a token of the all-BF16 cache; bulk and one-token appends) sets
+    # MLAQ_DEV_RANGE in the writer; decoding the batch leaves the other
+    # sequences exact.
+    from bit_mla_kv_gb300.mlaq import DEV_RANGE
+    lens = [300, 500, 700]
+    case = Case(mode, [L + 1 for L in lens] if where == "ring_small_append" else lens, 16, seed=33)
+    b_bad, t_bad = {"ring": (0, 299), "packed": (1, 100), "ring_small_append": (0, 300), "page": (1, 100)}[where]
+    case.c[int(case.cu[b_bad]) + t_bad, 7] = 1e5
+    if where == "ring_small_append":
+        last = torch.tensor([int(case.cu[b + 1]) - 1 for b in range(case.B)])
+        keep = torch.ones(int(case.cu[-1]), dtype=torch.bool)
+        keep[last] = False
+        full_c, full_k, full_cu = case.c, case.k, case.cu
+        case.c, case.k = full_c[keep], full_k[keep]
+        case.cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+        case.build()
+        assert case.cache.device_status() == 0
+        case.cache.append(case.pt_d, case.seq_d, full_c[last].view(case.B, 1, 512).cuda().contiguous(),
+                          full_k[last].view(case.B, 1, 64).cuda().contiguous())
+        case.c, case.k, case.cu = full_c, full_k, full_cu
+    else:
+        case.build()
+    assert case.cache.device_status() & DEV_RANGE
+    case.cache.clear_status()
+    out, lse = case.decode()
+    for b in range(case.B):
+        if b != b_bad:
+            ro, rl = case.oracle_seq(b)
+            assert_close_out(out[b], lse[b], ro, rl, f"{mode} {where} seq {b}")
+
+
+def test_fp16_range_is_checked_for_queries():
+    from bit_mla_kv_gb300.mlaq import DEV_RANGE
+    case = Case("C4R4", [300, 500, 700], 32, seed=34)
+    case.ql[2, 21, 17] = 1e5   # one element of one head (in the second 16-head half)
+    case.build()
+    assert case.cache.device_status() == 0
+    out, lse = case.decode()
+    assert case.cache.device_status() & DEV_RANGE
+    for b in (0, 1):
+        ro, rl = case.oracle_seq(b)
+        assert_close_out(out[b], lse[b], ro, rl, f"seq {b}")
+
+
+def test_error_response_through_the_library():
+    """The pages' error-response diagnosis (reading R8; ai.info "Methodology
+    in Plain English" and "Main Findings": perturb one path's cache to NMSE
+    0.01 and measure the output's NMSE per unit of cache NMSE), computed with
+    the library: the perturbed tokens go through mlaq_append into an all-BF16
+    cache, mlaq_decode runs on the clean and the perturbed cache, and the
+    response is NMSE(out_perturbed, out_clean) / 0.01 over all heads. It must
+    agree with the oracle's path_response within 3% (the cache and the outputs
+    are rounded to bf16: about 0.4% per element, well under the 10%
+    per-element perturbation)."""
+    from bit_mla_kv_gb300.mlaq import Cache
+    lens = [1024, 4096]
+    base = Case("BF16", lens, 16, seed=5)
+    rng = np.random.default_rng(5)
+    for path, lo, hi in (("content", 0, 512), ("rope", 512, 576)):
+        noises = [rng.standard_normal((L, hi - lo)) for L in lens]
+        pert = base.c.float().clone(), base.k.float().clone()
+        for b, L in enumerate(lens):
+            a = int(base.cu[b])
+            x = torch.cat([pert[0], pert[1]], -1)[a:a + L, lo:hi].double()
+            n = torch.from_numpy(noises[b])
+            d = n * torch.sqrt(0.01 * (x * x).sum() / (n * n).sum())   # ||d||^2 / ||x||^2 = 0.01
+            if path == "content":
+                pert[0][a:a + L] = (x + d).float()
+            else:
+                pert[1][a:a + L] = (x + d).float()
+        outs = []
+        for c, k in ((base.c, base.k), (pert[0].to(torch.bfloat16), pert[1].to(torch.bfloat16))):
+            cache = Cache("BF16", base.num_pages, base.B, base.page_table.shape[1], max_heads=16)
+            pt = base.page_table.cuda()
+            seq = torch.zeros(base.B, dtype=torch.int32, device="cuda")
+            cache.append(pt, seq, c.cuda().contiguous(), k.cuda().contiguous(), cu_new=base.cu.cuda())
+            out, _ = cache.decode(base.ql.cuda().contiguous(), base.qr.cuda().contiguous(), pt, seq, base.scale)
+            assert cache.device_status() == 0
+            outs.append(out.double().cpu())
+        for b, L in enumerate(lens):
+            got = float(((outs[1][b] - outs[0][b]) ** 2).sum() / (outs[0][b] ** 2).sum()) / 0.01
+            want = O.path_response(base.ql[b].float().numpy(), base.qr[b].float().numpy(), base.tokens(b),
+                                   base.scale, path, noises[b])
+            assert abs(got - want) <= 0.03 * want, (path, b, got, want)
+
+
+@pytest.mark.parametrize("mode", ["C4R4", "C2R4", "BF16"])
+def test_cache_bytes_matches_oracle(mode):
+    """The library's persistent-cache accounting (mlaq_cache_bytes: BF16
+    buffers + packed copies + page mapping, onedev.kr system-efficiency
+    paragraph) equals the oracle's for single lengths and a mixed batch, and
+    the C4R4 ratios sit within 2% of the pages' 3.22x (4K) and 3.59x (128K)."""
+    import json
+    import os
+    from bit_mla_kv_gb300.mlaq import Cache
+    cache = Cache(mode, 1, 16, 2048, max_heads=16)
+    for lens in ([1], [132], [4096], [131072], [0, 1, 63, 64, 65, 132, 133, 4096, 131072, 7777]):
+        assert cache.cache_bytes(lens) == O.cache_bytes(lens, mode), (mode, lens)
+    if mode == "C4R4":
+        g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "compression.json")))
+        for L, published in g["ratios"].items():
+            pol, ref = cache.cache_bytes([int(L)])
+            assert abs(ref / pol - published) / published < 0.02, (L, ref / pol, published)
+
+
+@pytest.mark.parametrize("H,lens", [(32, [32768, 30000]), (128, [20000] * 4)])
+def test_decode_max_ctas_fills_partial_rows(H, lens):
+    # 1024 decode CTAs over sequences long enough that the plan makes about
+    # one item per CTA: the split partials reach the workspace's row bound
+    # (items * H up to B * H + 32768 + H), which must hold them all.
+    case = Case("C4R4", lens, H, seed=17)
+    case.build()
+    case.cache.set_decode_ctas(1024)
+    out, lse = case.decode()
+    assert case.cache.device_status() == 0
+    for b in range(case.B):
+        ro, rl = case.oracle_seq(b)
+        assert_close_out(out[b], lse[b], ro, rl, f"H={H} seq {b}")
+
+
 @pytest.mark.parametrize("mode,Q,H", [("C4R4", 2, 16), ("C4R4", 4, 16), ("C2R4", 2, 32), ("BF16", 3, 16)])
 def test_decode_multi_token_causal(mode, Q, H):
     # Q query tokens per sequence after their Q tokens were appended: query j
