@@ -261,12 +261,13 @@ class Workbench:
     """One workload on one device: its seeded inputs, a cache filled by the
     fused writer, and the step (append one token per sequence + decode)."""
 
-    def __init__(self, wl, rank, device, total_steps):
+    def __init__(self, wl, rank, device, total_steps, variant=0):
         from bit_mla_kv_gb300.mlaq import Cache
         self.wl, self.device = wl, device
         self.inp = build_inputs(wl, rank, device, total_steps)
         self.cache = Cache(wl.mode, self.inp["num_pages"], wl.B, self.inp["pt"].shape[1], max_heads=max(wl.H, 16),
                            device=device)
+        self.cache.set_decode_variant(variant)
         self.seq = torch.zeros(wl.B, dtype=torch.int32, device=device)
         self.cu_d = self.inp["cu"].to(device)
         self.out = torch.empty(wl.B, wl.H, 512, dtype=torch.bfloat16, device=device)
@@ -388,13 +389,13 @@ def measure_steps(wb, K, Wm, l2_flush, ws, device, first_step=0):
 PER_CONFIG_DEFAULT = "v2lite_c2r4,v2lite_bf16,v3_c4r4,long_c2r4,long_c4r4,long_bf16,serving_c4r4"
 
 
-def run_per_config(names, K, Wm, l2_flush, ws, rank, device, local):
+def run_per_config(names, K, Wm, l2_flush, ws, rank, device, local, variant=0):
     """The other workloads, each with its own cache, K timed steps and its own
     clock record; one line of numbers per workload."""
     res = {}
     for name in names:
         wl = W.workload(name)
-        wb = Workbench(wl, rank, device, Wm + 2 * K)
+        wb = Workbench(wl, rank, device, Wm + 2 * K, variant)
         pre = wb.prefill()
         sampler = ClockSampler(local)
         sampler.start()
@@ -430,7 +431,7 @@ def run_mlaq(args, ws, rank, local):
     torch.cuda.set_device(device)
     wl = W.workload(args.workload)
     K, Wm = args.steps, args.warmup
-    wb = Workbench(wl, rank, device, Wm + 3 * K)  # warmup + timed + instrumented + e2e steps
+    wb = Workbench(wl, rank, device, Wm + 3 * K, args.decode_variant)  # warmup + timed + instrumented + e2e steps
     prefill = wb.prefill()
     l2_flush = make_l2_flush(device)
     inp, cache, seq, out, lse = wb.inp, wb.cache, wb.seq, wb.out, wb.lse
@@ -530,7 +531,8 @@ def run_mlaq(args, ws, rank, local):
     per_config = None
     names = [n for n in args.per_config.split(",") if n and n != "none" and n != args.workload]
     if names:
-        per_config = run_per_config(names, args.per_config_steps, 3, l2_flush, ws, rank, device, local)
+        per_config = run_per_config(names, args.per_config_steps, 3, l2_flush, ws, rank, device, local,
+                                    args.decode_variant)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -551,6 +553,7 @@ def run_mlaq(args, ws, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "f16 MMA operands (int4/int2 codes exact), f32 accumulate",
         "data": "synthetic (seeded; N(0,1) latent with 8 outlier channels x10, RoPE pairs x10^U(-1,1))",
         "config": {"workload": f"{wl.name}: {wl.description}", "mode": wl.mode, "B": wl.B, "H": wl.H,
+                   "decode_variant": args.decode_variant,
                    "tokens_at_start": sum(lens_at_start), "step": "mlaq_append (1 token/seq) + mlaq_decode",
                    "l2": "flushed between timed steps, outside the step events: 256 MiB written, then 256 MiB of another buffer read so the flush leaves no dirty lines",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
@@ -634,6 +637,8 @@ def main():
     ap.add_argument("--per-config", default=PER_CONFIG_DEFAULT,
                     help="comma-separated other workloads measured after the headline ('none' to skip)")
     ap.add_argument("--per-config-steps", type=int, default=10)
+    ap.add_argument("--decode-variant", type=int, default=0, choices=[0, 1, 2],
+                    help="attention kernel: 0 automatic, 1 register scores, 2 tcgen05 scores")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

@@ -21,7 +21,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
     Extra nvcc flags (e.g. -DMLAQ_CTAS_PER_SM=3 -DMLAQ_STAGES=2 for the decode
     kernel's occupancy and staging depth) may be given in MLAQ_NVCC_FLAGS."""
     srcs = [os.path.join(HERE, "csrc", s) for s in SOURCES]
-    deps = srcs + [os.path.join(HERE, "csrc", "mlaq_internal.cuh"),
+    deps = srcs + [os.path.join(HERE, "csrc", "mlaq_internal.cuh"), os.path.join(HERE, "csrc", "mlaq_decode_tc.cuh"),
                    os.path.join(HERE, "..", "include", "mlaq.h")]
     extra = os.environ.get("MLAQ_NVCC_FLAGS", "").split()
     if extra:

@@ -269,6 +269,14 @@ int mlaq_set_decode_ctas(mlaq_cache* c, int32_t ctas) {
   if (!c) return MLAQ_ERR_NULL;
   if (ctas <= 0 || ctas > kMaxPlanCtas) return MLAQ_ERR_SHAPE;
   c->decode_ctas = ctas;
+  c->decode_ctas_set = 1;
+  return MLAQ_OK;
+}
+
+int mlaq_set_decode_variant(mlaq_cache* c, int32_t variant) {
+  if (!c) return MLAQ_ERR_NULL;
+  if (variant < 0 || variant > 2) return MLAQ_ERR_SHAPE;
+  c->decode_variant = variant;
   return MLAQ_OK;
 }
 

@@ -1328,7 +1328,12 @@ __global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(Deco
   if (w == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// ---------------------------------------------------------------------------
+}  // namespace mlaq
+
+#include "mlaq_decode_tc.cuh"
+
+namespace mlaq {
+
 // ---------------------------------------------------------------------------
 // Combine (split-KV): for every sequence with more than one item, the
 // normalized partials O_k and their lse_k merge into
@@ -1454,10 +1459,18 @@ static cudaError_t set_decode_attr() {
   return cudaFuncSetAttribute(decode_kernel<MODE, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)sizeof(DecodeSmem<NH>));
 }
+template <int MODE, int NH>
+static cudaError_t set_decode_tc_attr() {
+  return cudaFuncSetAttribute(decode_tc_kernel<MODE, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sizeof(TcSmem<NH>));
+}
 static cudaError_t set_all_decode_attrs() {
   const cudaError_t es[] = {
       set_decode_attr<MLAQ_C4R4, 16>(), set_decode_attr<MLAQ_C2R4, 16>(), set_decode_attr<MLAQ_BF16, 16>(),
       set_decode_attr<MLAQ_C4R4, 32>(), set_decode_attr<MLAQ_C2R4, 32>(), set_decode_attr<MLAQ_BF16, 32>(),
+      set_decode_tc_attr<MLAQ_C4R4, 16>(), set_decode_tc_attr<MLAQ_C2R4, 16>(), set_decode_tc_attr<MLAQ_BF16, 16>(),
+      set_decode_tc_attr<MLAQ_C4R4, 32>(), set_decode_tc_attr<MLAQ_C2R4, 32>(), set_decode_tc_attr<MLAQ_BF16, 32>(),
+      set_decode_tc_attr<MLAQ_C4R4, 64>(), set_decode_tc_attr<MLAQ_C2R4, 64>(), set_decode_tc_attr<MLAQ_BF16, 64>(),
       // the planner's shared-memory arrays exceed 48 KB for large batches
       cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)plan_smem_bytes(kMaxSeqs, kMaxPlanCtas))};
@@ -1480,13 +1493,9 @@ cudaError_t decode_attrs_ready() {
   return e;
 }
 
-template <int MODE, int NH>
-static cudaError_t run_decode(mlaq_cache* c, const DecodeParams& p, int grid_cta, cudaStream_t s) {
-  const int smem = (int)sizeof(DecodeSmem<NH>);
-  cudaEvent_t* ev = nullptr;
-  if (c->timing_events && c->timing_n < c->timing_max)
-    ev = reinterpret_cast<cudaEvent_t*>(c->timing_events) + 2 * c->timing_n;  // ev[0] precedes the plan
-  cudaError_t e = launch_pdl(decode_kernel<MODE, NH>, dim3(p.HB, grid_cta), dim3(kThreads), smem, s, p);
+// The combine after the attention kernel, and the call's closing event.
+static cudaError_t launch_combine(mlaq_cache* c, const DecodeParams& p, cudaStream_t s, cudaError_t e,
+                                  cudaEvent_t* ev) {
   if (e == cudaSuccess) {
     // one unit per CTA, every unit's partial loads in one round trip; large
     // batches take the 16-channel units so that the grid stays near one wave
@@ -1503,16 +1512,42 @@ static cudaError_t run_decode(mlaq_cache* c, const DecodeParams& p, int grid_cta
   return e;
 }
 
+template <int MODE, int NH>
+static cudaError_t run_decode_tc(mlaq_cache* c, const DecodeParams& p, int grid_cta, cudaStream_t s) {
+  cudaEvent_t* ev = nullptr;
+  if (c->timing_events && c->timing_n < c->timing_max)
+    ev = reinterpret_cast<cudaEvent_t*>(c->timing_events) + 2 * c->timing_n;  // ev[0] precedes the plan
+  const cudaError_t e = launch_pdl(decode_tc_kernel<MODE, NH>, dim3(p.HB, grid_cta), dim3(TcCfg<NH>::kThreads),
+                                   sizeof(TcSmem<NH>), s, p);
+  return launch_combine(c, p, s, e, ev);
+}
+
+template <int MODE, int NH>
+static cudaError_t run_decode(mlaq_cache* c, const DecodeParams& p, int grid_cta, cudaStream_t s) {
+  const int smem = (int)sizeof(DecodeSmem<NH>);
+  cudaEvent_t* ev = nullptr;
+  if (c->timing_events && c->timing_n < c->timing_max)
+    ev = reinterpret_cast<cudaEvent_t*>(c->timing_events) + 2 * c->timing_n;  // ev[0] precedes the plan
+  const cudaError_t e = launch_pdl(decode_kernel<MODE, NH>, dim3(p.HB, grid_cta), dim3(kThreads), smem, s, p);
+  return launch_combine(c, p, s, e, ev);
+}
+
 cudaError_t launch_decode(mlaq_cache* c, const uint16_t* q_latent, const uint16_t* q_rope,
                           const int32_t* page_table, const int32_t* seq_lens, int B, int H, float scale,
                           uint16_t* out, float* lse, cudaStream_t s, int q_len) {
   char* ws = static_cast<char*>(c->workspace);
   const WsLayout lay = ws_layout(c->max_seqs, c->max_heads);
-  // heads per CTA: 32 when H allows it (one unpack per page for both halves)
-  const int NH = H % 32 == 0 ? 32 : 16;
+  // Kernel: the register-score kernel by default (measured faster on GB300
+  // for every head count; the tcgen05-score kernel is variant 2), with 32
+  // heads per CTA when H allows it (one unpack per page for both halves), 16
+  // otherwise; the tcgen05-score kernel with 64, 32 or 16 heads per CTA.
+  const bool tc = c->decode_variant == 2;
+  const int NH = tc ? (H % 64 == 0 ? 64 : H % 32 == 0 ? 32 : 16) : (H % 32 == 0 ? 32 : 16);
   const int HB = H / NH;
-  // item slots (CTAs per head block)
-  const int G = plan_slots(c->decode_ctas, HB, H);
+  // item slots (CTAs per head block): by default one wave of the kernel's
+  // resident CTAs (tcgen05 kernel: one per SM)
+  const int ctas = c->decode_ctas_set ? c->decode_ctas : (tc ? max(1, c->num_sms) : c->decode_ctas);
+  const int G = plan_slots(ctas, HB, H);
 
   DecodeParams p;
   p.codes = static_cast<const uint8_t*>(c->codes);
@@ -1559,6 +1594,21 @@ cudaError_t launch_decode(mlaq_cache* c, const uint16_t* q_latent, const uint16_
                              reinterpret_cast<int*>(ws + lay.cta_item_start),
                              reinterpret_cast<Item*>(ws + lay.cta_first), reinterpret_cast<int*>(ws + kWsNumItems));
   if (e != cudaSuccess) return e;
+  if (tc) {
+    if (NH == 64) {
+      if (c->mode == MLAQ_C4R4) return run_decode_tc<MLAQ_C4R4, 64>(c, p, G, s);
+      if (c->mode == MLAQ_C2R4) return run_decode_tc<MLAQ_C2R4, 64>(c, p, G, s);
+      return run_decode_tc<MLAQ_BF16, 64>(c, p, G, s);
+    }
+    if (NH == 32) {
+      if (c->mode == MLAQ_C4R4) return run_decode_tc<MLAQ_C4R4, 32>(c, p, G, s);
+      if (c->mode == MLAQ_C2R4) return run_decode_tc<MLAQ_C2R4, 32>(c, p, G, s);
+      return run_decode_tc<MLAQ_BF16, 32>(c, p, G, s);
+    }
+    if (c->mode == MLAQ_C4R4) return run_decode_tc<MLAQ_C4R4, 16>(c, p, G, s);
+    if (c->mode == MLAQ_C2R4) return run_decode_tc<MLAQ_C2R4, 16>(c, p, G, s);
+    return run_decode_tc<MLAQ_BF16, 16>(c, p, G, s);
+  }
   if (NH == 32) {
     if (c->mode == MLAQ_C4R4) return run_decode<MLAQ_C4R4, 32>(c, p, G, s);
     if (c->mode == MLAQ_C2R4) return run_decode<MLAQ_C2R4, 32>(c, p, G, s);

@@ -34,7 +34,7 @@ EXPORTED = [
     "mlaq_buffer_sizes", "mlaq_cache_create", "mlaq_cache_destroy", "mlaq_append", "mlaq_decode",
     "mlaq_export_tokens", "mlaq_cache_bytes", "mlaq_get_device_status", "mlaq_clear_device_status",
     "mlaq_timing_enable", "mlaq_timing_read", "mlaq_set_decode_ctas", "mlaq_set_plan_costs", "mlaq_status_string",
-    "mlaq_decode_noalloc", "mlaq_debug_wait_probe", "mlaq_decode_mtp",
+    "mlaq_decode_noalloc", "mlaq_debug_wait_probe", "mlaq_decode_mtp", "mlaq_set_decode_variant",
 ]
 
 _lib.mlaq_status_string.restype = ctypes.c_char_p
@@ -53,6 +53,7 @@ _lib.mlaq_timing_enable.argtypes = [_vp, _i32]
 _lib.mlaq_timing_read.argtypes = [_vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(_i32)]
 _lib.mlaq_set_decode_ctas.argtypes = [_vp, _i32]
 _lib.mlaq_set_plan_costs.argtypes = [_vp, _i32, _i32, _i32]
+_lib.mlaq_set_decode_variant.argtypes = [_vp, _i32]
 _lib.mlaq_decode_noalloc.argtypes = [ctypes.c_int, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _i32,
                                      ctypes.c_float, _vp, _vp, _vp, _vp]
 _lib.mlaq_debug_wait_probe.argtypes = [_vp, _i32, _i32, _vp]
@@ -282,6 +283,10 @@ class Cache:
 
     def set_decode_ctas(self, ctas: int):
         _check(_lib.mlaq_set_decode_ctas(self._h, ctas), "mlaq_set_decode_ctas")
+
+    def set_decode_variant(self, variant: int):
+        """0 automatic, 1 register-score kernel, 2 tcgen05-score kernel."""
+        _check(_lib.mlaq_set_decode_variant(self._h, variant), "mlaq_set_decode_variant")
 
     def set_plan_costs(self, step: int, ring: int, item: int):
         _check(_lib.mlaq_set_plan_costs(self._h, step, ring, item), "mlaq_set_plan_costs")

@@ -256,8 +256,22 @@ int mlaq_clear_device_status(mlaq_cache* cache, struct CUstream_st* stream);
 int mlaq_timing_enable(mlaq_cache* cache, int32_t max_calls);
 int mlaq_timing_read(mlaq_cache* cache, float* ms_out, int32_t* n);
 
-/* Number of CTAs the decode planner aims to fill (default 2 per SM). */
+/* Number of CTAs the decode planner aims to fill (default: one wave of the
+ * attention kernel's resident CTAs, 2 per SM for the register-score kernel,
+ * 1 per SM for the tcgen05-score kernel). 1 <= ctas <= 1024. */
 int mlaq_set_decode_ctas(mlaq_cache* cache, int32_t ctas);
+
+/* Which attention kernel mlaq_decode / mlaq_decode_mtp use (a tuning and
+ * test knob; results agree within the stated tolerances):
+ *   0 (default) automatic: currently the register-score kernel for every
+ *     head count (the faster one on GB300 for the tuned shapes);
+ *   1 register scores (legacy m16n8k16 MMAs on exact codes, tcgen05
+ *     aggregation);
+ *   2 tcgen05 scores and aggregation (64, 32 or 16 heads per CTA; exact
+ *     scores through split fp16 scales).
+ * MLAQ_ERR_SHAPE for other values. Host call; takes effect at the next
+ * decode. */
+int mlaq_set_decode_variant(mlaq_cache* cache, int32_t variant);
 
 /* Costs the decode planner balances across CTAs (a tuning knob; the results
  * do not depend on it): `step` per 16-token step of a packed page or BF16

@@ -354,13 +354,36 @@ def test_decode_max_ctas_fills_partial_rows(H, lens):
         assert_close_out(out[b], lse[b], ro, rl, f"H={H} seq {b}")
 
 
-@pytest.mark.parametrize("mode,Q,H", [("C4R4", 2, 16), ("C4R4", 4, 16), ("C2R4", 2, 32), ("BF16", 3, 16)])
-def test_decode_multi_token_causal(mode, Q, H):
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("mode,H", [("C4R4", 16), ("C4R4", 64), ("C4R4", 128), ("C2R4", 32), ("C2R4", 128),
+                                    ("BF16", 48), ("BF16", 64)])
+def test_decode_kernel_variants(mode, H, variant):
+    # Both attention kernels on every head blocking: register scores
+    # (variant 1) and tcgen05 scores (variant 2, 64 / 32 / 16 heads per CTA),
+    # with the default, a single and many splits per sequence.
+    case = Case(mode, [5, 140, 777, 2048, 4097], H, seed=51)
+    case.build()
+    case.cache.set_decode_variant(variant)
+    for ctas in (None, 1, 600):
+        if ctas is not None:
+            case.cache.set_decode_ctas(ctas)
+        out, lse = case.decode()
+        assert case.cache.device_status() == 0
+        for b in range(case.B):
+            ro, rl = case.oracle_seq(b)
+            assert_close_out(out[b], lse[b], ro, rl, f"{mode} H={H} variant {variant} ctas={ctas} seq {b}")
+
+
+@pytest.mark.parametrize("mode,Q,H,variant", [("C4R4", 2, 16, 0), ("C4R4", 4, 16, 0), ("C2R4", 2, 32, 0),
+                                              ("BF16", 3, 16, 0), ("C4R4", 4, 16, 2), ("C4R4", 2, 64, 0),
+                                              ("C2R4", 2, 32, 2), ("BF16", 3, 16, 2)])
+def test_decode_multi_token_causal(mode, Q, H, variant):
     # Q query tokens per sequence after their Q tokens were appended: query j
     # sees t < L - (Q - 1 - j). The lengths put the hidden tokens among the
     # sink slots (L <= 6), the recent ring and, in BF16 mode, the last page.
     case = Case(mode, [1, 2, 3, 6, 133, 140, 700, 3000], H, seed=40 + Q)
     case.build(max_heads=Q * H)
+    case.cache.set_decode_variant(variant)
     ql, qr = W.make_queries(case.B, Q * H, W.generator(90 + Q, "cpu"), "cpu")
     ql = ql.view(case.B, Q, H, 512).contiguous()
     qr = qr.view(case.B, Q, H, 64).contiguous()
@@ -380,24 +403,26 @@ def test_decode_multi_token_causal(mode, Q, H):
                 assert_close_out(out[b, j], lse[b, j], ro, rl, f"{mode} Q={Q} ctas={ctas} seq {b} query {j}")
 
 
-@pytest.mark.parametrize("mode", ["C4R4", "C2R4", "BF16"])
-def test_decode_running_max_rescale(mode):
+@pytest.mark.parametrize("mode,H,variant", [("C4R4", 16, 0), ("C2R4", 16, 0), ("BF16", 16, 0), ("C4R4", 64, 2),
+                                            ("C2R4", 16, 2), ("BF16", 64, 2)])
+def test_decode_running_max_rescale(mode, H, variant):
     # Later tokens carry larger latents, so the running max of every head
     # rises by far more than the lazy-rescale threshold partway through each
     # sequence: the accumulated output (TMEM or registers) must be rescaled
     # mid-item, in full-page and 16-token steps and across splits.
-    case = Case(mode, [700, 3000, 5000], 16, seed=22)
+    case = Case(mode, [700, 3000, 5000], H, seed=22)
     for b, L in enumerate(case.seq_lens):
         a = int(case.cu[b])
         for lo, f in ((L // 3, 3.0), (2 * L // 3, 6.0)):
             case.c[a + lo:a + L] = (case.c[a + lo:a + L].float() * f).to(torch.bfloat16)
     case.build()
+    case.cache.set_decode_variant(variant)
     for ctas in (1, 300):
         case.cache.set_decode_ctas(ctas)
         out, lse = case.decode()
         for b in range(case.B):
             ro, rl = case.oracle_seq(b)
-            assert_close_out(out[b], lse[b], ro, rl, f"{mode} ctas={ctas} seq {b}")
+            assert_close_out(out[b], lse[b], ro, rl, f"{mode} H={H} variant {variant} ctas={ctas} seq {b}")
 
 
 @pytest.mark.parametrize("costs", [(8, 19, 40), (1, 50, 0), (8, 1, 500), (3, 7, 100)])
