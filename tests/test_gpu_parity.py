@@ -83,6 +83,46 @@ def test_writer_exact_ties_round_half_to_even(mode):
         off += L
 
 
+@pytest.mark.parametrize("mode", ["C4R4", "C2R4"])
+def test_writer_odd_scale_midpoints_bit_exact(mode):
+    # Scales with an odd mantissa (3, 5 or 7 times a power of two, so 1/s is
+    # not exact in fp32) and values on code midpoints (x - mn)/s = k + 1/2, or
+    # one bf16 ulp beside them: the fp32 quotient must round exactly as the
+    # oracle's IEEE division does; 1000 rows take the bulk writer.
+    case = Case(mode, [600, 400], 16, seed=37)
+    n = sum(case.seq_lens)
+    rng = np.random.default_rng(37)
+    c = np.empty((n, 512), np.float32)
+    k = np.empty((n, 64), np.float32)
+    for arr, bits in ((c, 4 if mode == "C4R4" else 2), (k, 4)):
+        qmax = (1 << bits) - 1
+        for g in range(arr.shape[1] // 64):
+            s0 = rng.choice([3.0, 5.0, 7.0], size=n) * 2.0 ** rng.integers(-9, -2, size=n)
+            mn = rng.integers(-8, 8, size=n) * s0 / 2
+            vals = rng.integers(0, qmax, size=(n, 64)) + 0.5
+            x = mn[:, None] + vals * s0[:, None]
+            # one bf16 ulp away from the midpoint (away from or towards zero)
+            bits = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+            nudge = rng.random((n, 64))
+            step = np.where(nudge < 0.2, 1, np.where(nudge > 0.8, -1, 0)).astype(np.int16)
+            bits = np.where(x != 0, bits + step, bits).astype(np.int16)
+            x = torch.from_numpy(bits).view(torch.bfloat16).float().numpy().astype(np.float64)
+            x[:, 0] = mn               # the group minimum
+            x[:, 1] = mn + qmax * s0   # the group maximum: s = s0 exactly
+            arr[:, 64 * g:64 * g + 64] = x
+    case.c = torch.from_numpy(c).to(torch.bfloat16)
+    case.k = torch.from_numpy(k).to(torch.bfloat16)
+    case.build()
+    assert case.cache.device_status() == 0
+    codes, meta = _export_all(case)
+    off = 0
+    for b, L in enumerate(case.seq_lens):
+        ec, em = expected_codes(case, b)
+        np.testing.assert_array_equal(codes[off:off + L], ec, err_msg=f"codes seq {b}")
+        np.testing.assert_array_equal(meta[off:off + L].view(np.uint16), em.view(np.uint16), err_msg=f"meta seq {b}")
+        off += L
+
+
 @pytest.mark.parametrize("mode", ["C4R4", "C2R4", "BF16"])
 def test_writer_bulk_varlen_gaps_then_uniform(mode):
     # Two bulk appends on top of each other: a varlen call whose counts
