@@ -162,6 +162,12 @@ def test_quantize_tokens_group_layout_and_modes():
             np.testing.assert_array_equal(meta[:, g, 0], sg)
             np.testing.assert_array_equal(meta[:, g, 1], mg)
         assert np.all(meta[:, 8, 1] == k.min(-1).astype(np.float16))
+        # the RoPE group uses the RoPE width (4 bits in both modes), not the content width
+        assert br == 4
+        qr, sr, mr = O.quantize_groups(k, br)
+        np.testing.assert_array_equal(codes[:, 512:], qr)
+        np.testing.assert_array_equal(meta[:, 8, 0], sr)
+        np.testing.assert_array_equal(meta[:, 8, 1], mr)
 
 
 def test_quantization_is_per_token_no_requant():
