@@ -483,6 +483,32 @@ def test_plan_costs_change_only_the_split(costs):
         assert_close_out(out[b], lse[b], ro, rl, f"costs {costs} seq {b}")
 
 
+@pytest.mark.parametrize("B", [1000, 1100])
+def test_many_short_sequences_plan(B):
+    # Many short and empty sequences (around and above a thousand) put many
+    # items and empty sequences in one CTA range; forced CTA counts move every
+    # boundary. Empty sequences give out = 0 and lse = -inf.
+    rng = np.random.default_rng(40 + B)
+    lens = rng.choice([0, 0, 1, 3, 4, 5, 64, 65, 131, 132, 133, 200, 333], size=B)
+    lens[:3] = 0        # empty sequences first
+    lens[-2:] = 0       # and last
+    case = Case("C4R4", lens, 16, seed=41)
+    case.build()
+    check = sorted(set(rng.choice(B, size=40, replace=False).tolist()) | {0, 3, B - 3, B - 1})
+    for ctas in (None, 7, 600):
+        if ctas is not None:
+            case.cache.set_decode_ctas(ctas)
+        out, lse = case.decode()
+        assert case.cache.device_status() == 0
+        empty = torch.tensor(lens == 0, device=out.device)
+        assert torch.all(out[empty] == 0) and torch.all(torch.isneginf(lse[empty]))
+        for b in check:
+            if lens[b] == 0:
+                continue
+            ro, rl = case.oracle_seq(b)
+            assert_close_out(out[b], lse[b], ro, rl, f"B={B} ctas={ctas} seq {b} L={lens[b]}")
+
+
 def test_split_invariance():
     case = Case("C4R4", [3000, 9000, 133, 640], 16, seed=15)
     case.build()
