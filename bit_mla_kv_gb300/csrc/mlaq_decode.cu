@@ -511,8 +511,15 @@ __device__ void producer_advance(const DecodeParams& p, SM& sm, ProdCursor& pc, 
   pc.page = stage_page<MODE>(p, pc.cur, pc.k);
 }
 
+// Register budget of the attention kernel: a cap of 240 (two CTAs per SM
+// fit either way) measured 1-2% faster than the allocation that two CTAs per
+// SM as launch bounds give (221 registers).
+#ifndef MLAQ_DECODE_MAXNREG
+#define MLAQ_DECODE_MAXNREG 240
+#endif
+#define MLAQ_DECODE_BOUNDS __maxnreg__(MLAQ_DECODE_MAXNREG)
 template <int MODE, int NH>
-__global__ void __launch_bounds__(kThreads, MLAQ_CTAS_PER_SM) decode_kernel(DecodeParams p) {
+__global__ void MLAQ_DECODE_BOUNDS decode_kernel(DecodeParams p) {
   static_assert(NH == 16 || NH == 32, "16 or 32 heads per CTA");
   using SM = DecodeSmem<NH>;
   constexpr int kS = SM::kNumStages;
