@@ -18,9 +18,7 @@ def nvcc_path() -> str:
 def build(verbose: bool = False, force: bool = False) -> str:
     """Compile the CUDA sources into bit_mla_kv_gb300/libmlaq.so; returns its path.
 
-    Extra nvcc flags (e.g. -DMLAQ_STAGES=2 for the decode kernel's staging
-    depth, -DMLAQ_DECODE_MAXNREG=N for its register cap, with
-    -DMLAQ_CTAS_PER_SM=3 when N <= 168) may be given in MLAQ_NVCC_FLAGS."""
+    Extra nvcc flags (experiments) may be given in MLAQ_NVCC_FLAGS."""
     srcs = [os.path.join(HERE, "csrc", s) for s in SOURCES]
     deps = srcs + [os.path.join(HERE, "csrc", "mlaq_internal.cuh"), os.path.join(HERE, "csrc", "mlaq_decode_tc.cuh"),
                    os.path.join(HERE, "..", "include", "mlaq.h")]

@@ -91,7 +91,7 @@ int mlaq_cache_create(mlaq_cache** out, int mode, int32_t num_pages, int32_t max
   c->workspace = workspace;
   c->workspace_bytes = workspace_bytes;
   c->num_sms = sms;
-  c->decode_ctas = MLAQ_CTAS_PER_SM * sms < kMaxPlanCtas ? MLAQ_CTAS_PER_SM * sms : kMaxPlanCtas;
+  c->decode_ctas = 0;  // the kernel's own default (one wave) until mlaq_set_decode_ctas
   c->cost_step = kDefCostStep;
   c->cost_ring = kDefCostRing;
   c->cost_item = kDefCostItem;

@@ -49,7 +49,6 @@ namespace mlaq {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kStages = MLAQ_STAGES;
 constexpr int kT = 16;                                // tokens per step
 constexpr int kRingChunks = (kRing + kT - 1) / kT;    // 9
 constexpr int kStageBytes = kPage * 288 + kMetaPage;  // 20736: max(C4R4 page + meta, 16 BF16 tokens)
@@ -60,10 +59,24 @@ struct BoolC {
   static constexpr bool value = B;
 };
 // floats per row of partial scores [h][t]: 64 tokens of a page step + 4 (bank spread)
-constexpr int kSpStride = 68;
+// Per head count: a packed page is processed in 4 / subs bodies of `subs`
+// 16-token sub-steps each (one pair of barriers and one softmax per body).
+// 16-head CTAs take half pages: their TMEM (O^T 64 columns + A 64) and
+// shared memory (2 stages, 32-token score tiles) fit three CTAs per SM at 168
+// registers, which measured faster than whole pages at two CTAs per SM
+// (V2-Lite C4R4 110.4 vs 115.7 us per call). 32-head CTAs keep whole pages
+// at two per SM (O^T alone takes 128 columns).
+template <int NH>
+__host__ __device__ constexpr int body_subs() { return NH == 16 ? 2 : 4; }
+template <int NH>
+__host__ __device__ constexpr int ctas_per_sm() { return NH == 16 ? 3 : 2; }
+template <int NH>
+__host__ __device__ constexpr int sp_stride() { return 16 * body_subs<NH>() + 4; }  // floats per score row
 // Aggregation on tcgen05: O^T[channel][head] accumulates in TMEM.
 constexpr int kAggBufs = 2;      // A (content) / P^T step buffers in flight
-constexpr int kTmemCols = 256;   // O^T: 4 blocks x NH heads, then A: 4 sub-steps x 4 blocks x 8 columns
+// TMEM columns of a CTA: O^T (4 blocks x NH heads), then A (sub-steps x 4 blocks x 8 columns)
+template <int NH>
+__host__ __device__ constexpr uint32_t tmem_cols() { return 4 * NH + 32 * body_subs<NH>() <= 128 ? 128 : 256; }
 // first TMEM column of the A step buffers for NH heads per CTA
 template <int NH>
 __host__ __device__ constexpr uint32_t tmem_a_col() { return 4 * NH; }
@@ -97,25 +110,28 @@ struct DecodeParams {
 // for two stages at two CTAs per SM).
 template <int NH>
 struct __align__(128) DecodeSmem {
-  static constexpr int kNumStages = NH == 16 ? kStages : 2;
+  static constexpr int kNumStages = 2;
   static constexpr int kQxWords = NH == 16 ? 1 : 10 * kThreads;  // 38 fragment words per thread, as uint4
   uint8_t stage[kNumStages][kStageBytes];
-  float sp[kWarps][NH][kSpStride];  // partial scores, [warp][head][token]
+  float sp[kWarps][NH][sp_stride<NH>()];  // partial scores, [warp][head][token]
   float alpha[NH];
   float fin_m[NH];
   float fin_l[NH];
   int stage_bad[kNumStages];
   uint64_t full[kNumStages];
   __align__(128) uint8_t pt[kAggBufs][32 * NH];  // P^T B operand: NH heads x 16 tokens, 8x8 core matrices
-  __align__(128) uint8_t ptp[4][32 * NH];        // P^T of the four sub-steps of a page step
+  __align__(128) uint8_t ptp[body_subs<NH>()][32 * NH];  // P^T of the sub-steps of a page body
   uint64_t agg_done[kAggBufs];
   uint32_t tmem_base;
   int rescale_flag[kWarps];
   uint4 qx[kQxWords];  // query fragments of heads 16..31 of the block, [word / 4][thread]
 };
-// two CTAs per SM: 228 KB of shared memory, 1 KB of it reserved per CTA
-static_assert(sizeof(DecodeSmem<16>) <= 113 * 1024 && sizeof(DecodeSmem<32>) <= 113 * 1024,
-              "decode shared memory must allow two CTAs per SM");
+// ctas_per_sm CTAs per SM: 228 KB of shared memory, 1 KB of it reserved per CTA
+static_assert(sizeof(DecodeSmem<16>) * ctas_per_sm<16>() + 1024 * ctas_per_sm<16>() <= 228 * 1024 &&
+                  sizeof(DecodeSmem<32>) * ctas_per_sm<32>() + 1024 * ctas_per_sm<32>() <= 228 * 1024,
+              "decode shared memory must allow ctas_per_sm CTAs per SM");
+static_assert(tmem_cols<16>() * ctas_per_sm<16>() <= 512 && tmem_cols<32>() * ctas_per_sm<32>() <= 512,
+              "decode TMEM must allow ctas_per_sm CTAs per SM");
 
 __device__ __forceinline__ int clamp_len(int L, int max_tokens) { return min(max(L, 0), max_tokens); }
 // Units of a sequence and its leading ring units.
@@ -511,20 +527,20 @@ __device__ void producer_advance(const DecodeParams& p, SM& sm, ProdCursor& pc, 
   pc.page = stage_page<MODE>(p, pc.cur, pc.k);
 }
 
-// Register budget of the attention kernel: a cap of 240 (two CTAs per SM
-// fit either way) measured 1-2% faster than the allocation that two CTAs per
-// SM as launch bounds give (221 registers).
-#ifndef MLAQ_DECODE_MAXNREG
-#define MLAQ_DECODE_MAXNREG 240
-#endif
-#define MLAQ_DECODE_BOUNDS __maxnreg__(MLAQ_DECODE_MAXNREG)
+// Register budget of the attention kernel: 168 for three 16-head CTAs per
+// SM (no spills), 240 for two 32-head CTAs (measured 1-2% faster than the 221
+// registers that two CTAs per SM as launch bounds give).
+template <int NH>
+__host__ __device__ constexpr int decode_maxnreg() { return NH == 16 ? 168 : 240; }
 template <int MODE, int NH>
-__global__ void MLAQ_DECODE_BOUNDS decode_kernel(DecodeParams p) {
+__global__ void __maxnreg__(decode_maxnreg<NH>()) decode_kernel(DecodeParams p) {
   static_assert(NH == 16 || NH == 32, "16 or 32 heads per CTA");
   using SM = DecodeSmem<NH>;
   constexpr int kS = SM::kNumStages;
   constexpr int NP = NH / 16;                       // 16-head halves sharing each unpack
   constexpr uint32_t kTmemA = tmem_a_col<NH>();
+  constexpr int kSubs = body_subs<NH>();      // sub-steps per page body
+  constexpr int kPageParts = 4 / kSubs;        // page bodies per packed page
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SM& sm = *reinterpret_cast<SM*>(smem_raw);
   const int cta = blockIdx.y;
@@ -551,7 +567,7 @@ __global__ void MLAQ_DECODE_BOUNDS decode_kernel(DecodeParams p) {
     fence_proxy_async();
   }
   if (w == 0) {
-    tmem_alloc(&sm.tmem_base, kTmemCols);
+    tmem_alloc(&sm.tmem_base, tmem_cols<NH>());
     tmem_relinquish();
   }
   tc_fence_before();
@@ -1032,7 +1048,7 @@ __global__ void MLAQ_DECODE_BOUNDS decode_kernel(DecodeParams p) {
       // O^T += V^T P^T asynchronously.
       // MASKED: rows outside the packed range [4, L - 128) contribute nothing
       // (zero scale and min, score -inf); the first and last pages of a range.
-      auto page_body = [&](auto masked_c) -> bool {
+      auto page_body = [&](auto masked_c, const int part) -> bool {
         constexpr bool MASKED = decltype(masked_c)::value;
         bool agg_ok = true;
         if (agg_ctr > 0) {  // every earlier aggregation MMA has read its TMEM/smem operands
@@ -1042,8 +1058,8 @@ __global__ void MLAQ_DECODE_BOUNDS decode_kernel(DecodeParams p) {
         tc_fence_after();
         const uint8_t* mtab = st + page_code_bytes(MODE);
 #pragma unroll 1
-        for (int sub = 0; sub < 4; ++sub) {
-          const int lr = 16 * sub + r;
+        for (int sub = 0; sub < kSubs; ++sub) {
+          const int lr = 16 * (kSubs * part + sub) + r;
           bool v0 = true, v1 = true;
           if constexpr (MASKED) {
             const int t = kPage * sref.idx + lr;
@@ -1133,37 +1149,36 @@ __global__ void MLAQ_DECODE_BOUNDS decode_kernel(DecodeParams p) {
         tc_fence_before();
         // barrier 1: partial scores and A tiles complete; agrees on a timed-out wait
         if (named_bar_or(1, kThreads, !(ok && agg_ok))) return true;
-        if (tid == 0) producer_advance<MODE>(p, sm, pc, i1);
-        // online softmax for heads hh (+ 16), tokens tq .. tq + 3 and 32 + tq .. 32 + tq + 3
-        // (a quarter warp reads 128 contiguous bytes of a score row)
+        if (tid == 0 && part == kPageParts - 1) producer_advance<MODE>(p, sm, pc, i1);
+        // online softmax for heads hh (+ 16), tokens tq .. tq + 3 (and 32 + tq .. 32 + tq + 3
+        // in whole pages) of the body (a quarter warp reads 128 contiguous bytes of a score row)
         {
+          constexpr int NU = 2 * kSubs;  // tokens per thread
           const int tq = 4 * (lane & 7);
           bool rs = false;
 #pragma unroll
           for (int hp = 0; hp < NP; ++hp) {
             const int hq = hh + 16 * hp;
-            float x[8];
+            float x[NU];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) x[u] = 0.f;
+            for (int u = 0; u < NU; ++u) x[u] = 0.f;
 #pragma unroll
             for (int ww = 0; ww < kWarps; ++ww) {
-              const float4 v0 = *reinterpret_cast<const float4*>(&sm.sp[ww][hq][tq]);
-              const float4 v1 = *reinterpret_cast<const float4*>(&sm.sp[ww][hq][tq + 32]);
-              x[0] += v0.x;
-              x[1] += v0.y;
-              x[2] += v0.z;
-              x[3] += v0.w;
-              x[4] += v1.x;
-              x[5] += v1.y;
-              x[6] += v1.z;
-              x[7] += v1.w;
+#pragma unroll
+              for (int u4 = 0; u4 < NU; u4 += 4) {
+                const float4 v = *reinterpret_cast<const float4*>(&sm.sp[ww][hq][tq + 8 * u4]);
+                x[u4] += v.x;
+                x[u4 + 1] += v.y;
+                x[u4 + 2] += v.z;
+                x[u4 + 3] += v.w;
+              }
             }
             float xm = -INFINITY;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < NU; ++u) {
               bool valid = true;
               if constexpr (MASKED) {
-                const int t = kPage * sref.idx + tq + (u < 4 ? u : 28 + u);
+                const int t = kPage * sref.idx + 16 * kSubs * part + tq + (u < 4 ? u : 28 + u);
                 valid = (t >= kSink) & (t < L - kRecent);
               }
               x[u] = valid ? x[u] * p.scale_log2 : -INFINITY;
@@ -1182,10 +1197,10 @@ __global__ void MLAQ_DECODE_BOUNDS decode_kernel(DecodeParams p) {
             float psum = 0.f;
             const float mref = (MASKED && m_run[hp] == -INFINITY) ? 0.f : m_run[hp];  // nothing valid yet: p = 0
 #pragma unroll
-            for (int u = 0; u < 8; u += 2) {
+            for (int u = 0; u < NU; u += 2) {
               const float pa = ex2(x[u] - mref), pb = ex2(x[u + 1] - mref);
               psum += pa + pb;
-              const int tp64 = tq + (u < 4 ? u : 28 + u);  // token pair tp64, tp64 + 1 of the page
+              const int tp64 = tq + (u < 4 ? u : 28 + u);  // token pair tp64, tp64 + 1 of the body
               const int sub = tp64 >> 4, t = tp64 & 15;
               const int kp = t < 8 ? 2 * t : 2 * t - 14;  // their K index in the TMEM A columns
               const int off = (hq >> 3) * 256 + (kp >> 3) * 128 + (hq & 7) * 16 + (kp & 7) * 2;
@@ -1212,7 +1227,7 @@ __global__ void MLAQ_DECODE_BOUNDS decode_kernel(DecodeParams p) {
           if (lane == 0) {
             tc_fence_after();
 #pragma unroll
-            for (int sub = 0; sub < 4; ++sub) {
+            for (int sub = 0; sub < kSubs; ++sub) {
               const uint64_t bdesc = umma_smem_desc(smem_u32(sm.ptp[sub]), 128, 256);
               umma_f16_ts(tmem + (uint32_t)(NH * w), tmem + (uint32_t)(kTmemA + 32 * sub + 8 * w), bdesc,
                           kAggIdesc, !item_first || sub > 0);
@@ -1231,9 +1246,12 @@ __global__ void MLAQ_DECODE_BOUNDS decode_kernel(DecodeParams p) {
           const int t0 = kPage * sref.idx;
           if (!bad) {  // CTA-uniform
             const bool full = t0 >= kSink && t0 + kPage <= L - kRecent;
-            if (full ? page_body(BoolC<false>{}) : page_body(BoolC<true>{})) {
-              failed = true;
-              g_fail = g - 1;
+            for (int part = 0; part < kPageParts; ++part) {
+              if (full ? page_body(BoolC<false>{}, part) : page_body(BoolC<true>{}, part)) {
+                failed = true;
+                g_fail = g - 1;
+                break;
+              }
             }
             continue;
           }
@@ -1332,7 +1350,7 @@ __global__ void MLAQ_DECODE_BOUNDS decode_kernel(DecodeParams p) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (w == 0) tmem_dealloc(tmem, kTmemCols);
+  if (w == 0) tmem_dealloc(tmem, tmem_cols<NH>());
 }
 
 }  // namespace mlaq
@@ -1553,7 +1571,10 @@ cudaError_t launch_decode(mlaq_cache* c, const uint16_t* q_latent, const uint16_
   const int HB = H / NH;
   // item slots (CTAs per head block): by default one wave of the kernel's
   // resident CTAs (tcgen05 kernel: one per SM)
-  const int ctas = c->decode_ctas_set ? c->decode_ctas : (tc ? max(1, c->num_sms) : c->decode_ctas);
+  const int ctas = c->decode_ctas_set ? c->decode_ctas
+                   : tc              ? max(1, c->num_sms)
+                                     : min(kMaxPlanCtas, (NH == 16 ? ctas_per_sm<16>() : ctas_per_sm<32>()) *
+                                                              max(1, c->num_sms));
   const int G = plan_slots(ctas, HB, H);
 
   DecodeParams p;
@@ -1696,7 +1717,6 @@ int launch_decode_static(int mode, const void* codes, const void* meta, const vo
   c.workspace = g_static_ptr[dev];
   c.workspace_bytes = kStaticScratchBytes;
   c.num_sms = g_static_sms[dev];
-  c.decode_ctas = MLAQ_CTAS_PER_SM * c.num_sms < kMaxPlanCtas ? MLAQ_CTAS_PER_SM * c.num_sms : kMaxPlanCtas;
   c.cost_step = kDefCostStep;
   c.cost_ring = kDefCostRing;
   c.cost_item = kDefCostItem;

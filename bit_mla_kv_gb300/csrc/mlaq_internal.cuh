@@ -8,14 +8,6 @@
 
 #include "../../include/mlaq.h"
 
-// Decode kernel occupancy and staging depth (compile-time tuning knobs).
-#ifndef MLAQ_CTAS_PER_SM
-#define MLAQ_CTAS_PER_SM 2
-#endif
-#ifndef MLAQ_STAGES
-#define MLAQ_STAGES 4
-#endif
-
 namespace mlaq {
 
 constexpr int kPage = 64;        // tokens per page

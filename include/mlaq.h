@@ -257,8 +257,9 @@ int mlaq_timing_enable(mlaq_cache* cache, int32_t max_calls);
 int mlaq_timing_read(mlaq_cache* cache, float* ms_out, int32_t* n);
 
 /* Number of CTAs the decode planner aims to fill (default: one wave of the
- * attention kernel's resident CTAs, 2 per SM for the register-score kernel,
- * 1 per SM for the tcgen05-score kernel). 1 <= ctas <= 1024. */
+ * attention kernel's resident CTAs: for the register-score kernel 3 per SM
+ * with 16 heads per CTA, 2 per SM with 32; 1 per SM for the tcgen05-score
+ * kernel). 1 <= ctas <= 1024. */
 int mlaq_set_decode_ctas(mlaq_cache* cache, int32_t ctas);
 
 /* Which attention kernel mlaq_decode / mlaq_decode_mtp use (a tuning and
