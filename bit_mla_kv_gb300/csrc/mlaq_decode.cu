@@ -66,6 +66,9 @@ struct BoolC {
 // registers, which measured faster than whole pages at two CTAs per SM
 // (V2-Lite C4R4 110.4 vs 115.7 us per call). 32-head CTAs keep whole pages
 // at two per SM (O^T alone takes 128 columns).
+// (Measured alternatives for 16-head CTAs on V2-Lite C4R4: four per SM at 128
+// registers, 60 bytes of spills: 117.5 us; three stages: 111.8 us; against
+// 110.5 us for three per SM, 168 registers, two stages.)
 template <int NH>
 __host__ __device__ constexpr int body_subs() { return NH == 16 ? 2 : 4; }
 template <int NH>
