@@ -105,6 +105,9 @@ struct DecodeParams {
   int q_len, h_per_q;  // query tokens per sequence; heads per query token (H = q_len * h_per_q)
   int cost_step, cost_ring, cost_item;  // planning costs
   float scale_log2;
+  // CTA shares by dispatch slot (linear CTA index / SMs): relative speeds x
+  // 1000 of the first, second and third CTA resident on an SM
+  int sms, slot_w[3];
 };
 
 // Shared memory of a decode CTA serving NH heads (16, or 32 when H is a
@@ -196,6 +199,22 @@ __device__ int block_excl_scan(int v, int* red, int* total) {
   return warp_prefix + x - v;
 }
 
+// Weighted count of the item slots below c. Item slot c' of head block x is
+// linear CTA c' * HB + x, dispatched round-robin over the SMs, so it is the
+// (c' * HB / sms)-th CTA resident on its SM. The CTAs that share an SM run at
+// different speeds (the warps of the CTA dispatched first are scheduled
+// first): each gets a share of the cost in proportion to its slot's speed.
+__device__ __forceinline__ long long slot_weight_below(const DecodeParams& p, int c) {
+  long long w = 0;
+  int lo = 0;
+  for (int k = 0; k < 3; ++k) {
+    const int hi = k == 2 ? c : min(c, (int)(((long long)(k + 1) * p.sms + p.HB - 1) / p.HB));
+    if (hi > lo) w += (long long)(hi - lo) * p.slot_w[k];
+    lo = max(lo, hi);
+  }
+  return w;
+}
+
 // Largest index i in [lo, hi] with a[i] <= key (a non-decreasing, a[lo] <= key).
 __device__ __forceinline__ int last_le(const int* a, int lo, int hi, int key) {
   while (lo < hi) {
@@ -267,10 +286,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p, int mode, in
   if (tid == 0) useq[B] = carry_s;
   __syncthreads();
   const int U = useq[B];
-  // B: CTA boundaries (in cost), snapped down to a step start, and to a page
-  //    start inside packed pages.
+  // B: CTA boundaries (in cost): the slot-weighted share of c, snapped down
+  //    to a step start, and to a page start inside packed pages.
+  const long long w_all = slot_weight_below(p, G);
   for (int c = tid; c <= G; c += blockDim.x) {
-    const int raw = (int)(((long long)c * U) / G);
+    const int raw = c >= G ? U : (int)(((long long)U * slot_weight_below(p, c)) / w_all);
     int v = raw;
     if (raw < U) {
       const int b = last_le(useq, 0, B, raw);
@@ -1609,6 +1629,18 @@ cudaError_t launch_decode(mlaq_cache* c, const uint16_t* q_latent, const uint16_
   p.cost_step = c->cost_step;
   p.cost_ring = c->cost_ring;
   p.cost_item = c->cost_item;
+  // Shares of the first, second and third resident CTA of an SM. Per-CTA
+  // timing on GB300 (V2-Lite and serving C4R4 alike) gave 4.02, 4.24 and
+  // 4.44 us per page for three 16-head CTAs per SM at equal shares, and the
+  // later slots slow down further when they hold less: shares 1 : 0.925 :
+  // 0.86 measured best (serving 194.4 us per call against 199.8 at equal
+  // shares, V2-Lite 111.1 against 111.5). Two 32-head CTAs per SM differ by
+  // 1%; one tcgen05 CTA per SM has one slot.
+  p.sms = max(1, c->num_sms);
+  const bool three = !tc && NH == 16;
+  p.slot_w[0] = 1000;
+  p.slot_w[1] = three ? 925 : 1000;
+  p.slot_w[2] = three ? 860 : 1000;
 
   {
     const cudaError_t ea = decode_attrs_ready();
