@@ -138,6 +138,9 @@ static_assert(sizeof(DecodeSmem<16>) * ctas_per_sm<16>() + 1024 * ctas_per_sm<16
               "decode shared memory must allow ctas_per_sm CTAs per SM");
 static_assert(tmem_cols<16>() * ctas_per_sm<16>() <= 512 && tmem_cols<32>() * ctas_per_sm<32>() <= 512,
               "decode TMEM must allow ctas_per_sm CTAs per SM");
+// the page-body softmax reads its tokens four at a time (2 * subs per thread)
+static_assert((body_subs<16>() == 2 || body_subs<16>() == 4) && (body_subs<32>() == 2 || body_subs<32>() == 4),
+              "page bodies of two or four sub-steps");
 
 __device__ __forceinline__ int clamp_len(int L, int max_tokens) { return min(max(L, 0), max_tokens); }
 // Units of a sequence and its leading ring units.
