@@ -5,7 +5,8 @@ allocator, plugins that must not call cudaMalloc during stream capture,
 hosts that reserve all of HBM). For them the split-KV scratch lives in a
 fixed array inside the library. This test calls that entry point through the
 C ABI and checks it against mlaq_decode on the same cache, twice in a row
-(the second call reuses the array the first one left behind). It sits in a
+(the second call reuses the array the first one left behind), and against
+the oracle. It sits in a
 file collected last so that a stop-at-first-failure run has already run every
 other test; it passes alone in a fresh process as well.
 """
@@ -47,6 +48,11 @@ def test_noalloc_matches_decode_twice(mode, lens, H):
         for b in range(case.B):
             assert_close_out(out[b], lse[b], ref_out[b].float().cpu().double().numpy(),
                              ref_lse[b].cpu().double().numpy(), f"call {call} seq {b}")
+    # and directly against the oracle, so that a fault shared by both entry
+    # points (planner, attention kernel, combine) cannot pass unseen
+    for b in range(case.B):
+        ro, rl = case.oracle_seq(b)
+        assert_close_out(out[b], lse[b], ro, rl, f"oracle seq {b}")
 
 
 def _noalloc(m, cache, mode, ql, qr, pt, seq, B, H, scale, out, lse, st):
