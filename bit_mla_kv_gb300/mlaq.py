@@ -62,7 +62,7 @@ for _name in EXPORTED:
     if _name != "mlaq_status_string":
         getattr(_lib, _name).restype = ctypes.c_int
 
-DEV_PAGE_OOB, DEV_SEQ_OVERFLOW, DEV_NONFINITE, DEV_TIMEOUT, DEV_RANGE = 0x1, 0x2, 0x4, 0x8, 0x10
+DEV_PAGE_OOB, DEV_SEQ_OVERFLOW, DEV_NONFINITE, DEV_TIMEOUT, DEV_RANGE, DEV_BAD_ROWS = 0x1, 0x2, 0x4, 0x8, 0x10, 0x20
 
 
 class MlaqError(RuntimeError):

@@ -75,6 +75,8 @@ typedef enum mlaq_status {
 #define MLAQ_DEV_TIMEOUT 0x8      /* a bounded wait on a bulk copy ran out */
 #define MLAQ_DEV_RANGE 0x10       /* a value outside the decode's fp16 operand range
                                      (see mlaq_append and mlaq_decode) */
+#define MLAQ_DEV_BAD_ROWS 0x20    /* mlaq_append: cu_new[B] != total_new, or cu_new is
+                                     not a non-decreasing prefix sum from 0 */
 
 #define MLAQ_PAGE_TOKENS 64
 #define MLAQ_SINK 4
@@ -124,7 +126,10 @@ int mlaq_cache_destroy(mlaq_cache* cache);
  *   cu_new: NULL -> every sequence gets n_new tokens, rows laid out
  *       [B, n_new]; else a device int32 [B+1] prefix sum: sequence b gets rows
  *       cu_new[b] .. cu_new[b+1]-1, and total_new must equal cu_new[B]
- *       (the host value sizes the launch).
+ *       (the host value sizes the launch). A mismatch, or counts that are not
+ *       a non-decreasing prefix sum from 0, sets MLAQ_DEV_BAD_ROWS; rows that
+ *       cu_new does not place are skipped, and the lengths of such a call are
+ *       undefined (reset them before the next append).
  * Each token t is quantized per group (8 content groups + 1 RoPE group of 64
  * channels: mn = min, s = fp16((max - mn) / (2^b - 1)), q = clamp(rint((x -
  * fp16(mn)) / s), 0, 2^b - 1), s == 0 -> q = 0, IEEE fp32), packed into page

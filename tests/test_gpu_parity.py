@@ -169,6 +169,42 @@ def test_writer_bulk_varlen_gaps_then_uniform(mode):
         np.testing.assert_array_equal(ring[b][valid], er[valid], err_msg=f"ring seq {b} L={L}")
 
 
+@pytest.mark.parametrize("lens", [[100, 50], [700, 300]])
+@pytest.mark.parametrize("extra", [20, -30])
+def test_writer_flags_rows_cu_new_does_not_cover(lens, extra):
+    # total_new must equal cu_new[B]. More rows than cu_new places (extra >
+    # 0) or fewer (extra < 0) set MLAQ_DEV_BAD_ROWS instead of reading past
+    # cu_new and seq_lens; with more rows every placed row is still stored
+    # bit-exact. 150 rows take the one-CTA-per-row writer, 1000 the bulk one.
+    from bit_mla_kv_gb300.mlaq import Cache, DEV_BAD_ROWS
+    case = Case("C4R4", lens, 16, seed=43)
+    case.cache = Cache("C4R4", case.num_pages, case.B, case.page_table.shape[1], max_heads=16)
+    case.pt_d = case.page_table.cuda()
+    case.seq_d = torch.zeros(case.B, dtype=torch.int32, device="cuda")
+    n = sum(lens)
+    total = n + extra
+    gen = torch.Generator().manual_seed(43)
+    pad_c = torch.randn(max(extra, 0), 512, generator=gen).to(torch.bfloat16)
+    pad_k = torch.randn(max(extra, 0), 64, generator=gen).to(torch.bfloat16)
+    c = torch.cat([case.c, pad_c])[:total].cuda().contiguous()
+    k = torch.cat([case.k, pad_k])[:total].cuda().contiguous()
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device="cuda")
+    case.cache.append(case.pt_d, case.seq_d, c, k, cu_new=cu)
+    assert case.cache.device_status() & DEV_BAD_ROWS
+    case.cache.clear_status()
+    if extra > 0:
+        assert case.seq_d.cpu().tolist() == lens
+        codes, meta = _export_all(case)
+        off = 0
+        for b, L in enumerate(case.seq_lens):
+            ec, em = expected_codes(case, b)
+            np.testing.assert_array_equal(codes[off:off + L], ec, err_msg=f"codes seq {b}")
+            np.testing.assert_array_equal(meta[off:off + L].view(np.uint16), em.view(np.uint16),
+                                          err_msg=f"meta seq {b}")
+            off += L
+    assert case.cache.device_status() == 0
+
+
 def _extreme_groups(n, ncols, rng):
     """Rows whose 64-channel groups stress the quantizer's edge cases: tiny
     values (fp16-subnormal scales and minima that round), constant and
