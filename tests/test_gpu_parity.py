@@ -205,6 +205,63 @@ def test_writer_flags_rows_cu_new_does_not_cover(lens, extra):
     assert case.cache.device_status() == 0
 
 
+def test_positions_beyond_the_page_table_are_flagged():
+    # A page table with room for 128 tokens per sequence: the writer skips the
+    # rows of sequence 1 past position 127 and sets MLAQ_DEV_SEQ_OVERFLOW
+    # (the rows inside stay bit-exact); the planner clamps a length beyond the
+    # table, sets the same bit, and the other sequence decodes as usual.
+    from bit_mla_kv_gb300.mlaq import Cache, DEV_SEQ_OVERFLOW
+    lens = [100, 200]
+    case = Case("C4R4", lens, 16, seed=47)
+    pt = case.page_table[:, :2].contiguous()
+    case.cache = Cache("C4R4", case.num_pages, case.B, 2, max_heads=16)
+    case.pt_d = pt.cuda()
+    case.seq_d = torch.zeros(case.B, dtype=torch.int32, device="cuda")
+    case.cache.append(case.pt_d, case.seq_d, case.c.cuda().contiguous(), case.k.cuda().contiguous(),
+                      cu_new=case.cu.cuda())
+    assert case.cache.device_status() & DEV_SEQ_OVERFLOW
+    case.cache.clear_status()
+    for b, L in ((0, 100), (1, 128)):
+        tb = torch.full((L,), b, dtype=torch.int32, device="cuda")
+        tt = torch.arange(L, dtype=torch.int32, device="cuda")
+        codes, meta = case.cache.export_tokens(case.pt_d, tb, tt)
+        ec, em = expected_codes(case, b)
+        np.testing.assert_array_equal(codes.cpu().numpy(), ec[:L], err_msg=f"codes seq {b}")
+        np.testing.assert_array_equal(meta.cpu().numpy().view(np.uint16), em[:L].view(np.uint16),
+                                      err_msg=f"meta seq {b}")
+    assert case.cache.device_status() == 0
+    out, lse = case.decode()
+    assert case.cache.device_status() & DEV_SEQ_OVERFLOW
+    ro, rl = case.oracle_seq(0)
+    assert_close_out(out[0], lse[0], ro, rl, "sequence inside the table")
+
+
+@pytest.mark.parametrize("lens", [[700, 300], [1, 1]])
+def test_nonfinite_groups_are_flagged(lens):
+    # A NaN in one RoPE group and an infinity in one content group give
+    # non-finite (scale, min) metadata: MLAQ_DEV_NONFINITE, no fault, and
+    # every other token is still stored bit-exact (bulk and one-CTA writers).
+    from bit_mla_kv_gb300.mlaq import DEV_NONFINITE
+    case = Case("C4R4", lens, 16, seed=53)
+    a0, a1 = int(case.cu[0]) + lens[0] - 1, int(case.cu[1]) + lens[1] - 1   # last row of each sequence
+    case.k[a0, 7] = float("nan")
+    case.c[a1, 200] = float("inf")
+    case.build()
+    assert case.cache.device_status() & DEV_NONFINITE
+    case.cache.clear_status()
+    codes, meta = _export_all(case)
+    off = 0
+    for b, L in enumerate(case.seq_lens):
+        if L > 1:
+            tok = case.tokens(b)[:L - 1]   # the finite rows
+            ec, em = O.quantize_tokens(tok[:, :512], tok[:, 512:], case.mode)
+            np.testing.assert_array_equal(codes[off:off + L - 1], ec, err_msg=f"codes seq {b}")
+            np.testing.assert_array_equal(meta[off:off + L - 1].view(np.uint16), em.view(np.uint16),
+                                          err_msg=f"meta seq {b}")
+        off += L
+    assert case.cache.device_status() == 0
+
+
 def _extreme_groups(n, ncols, rng):
     """Rows whose 64-channel groups stress the quantizer's edge cases: tiny
     values (fp16-subnormal scales and minima that round), constant and
