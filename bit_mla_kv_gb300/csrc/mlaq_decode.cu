@@ -423,6 +423,15 @@ __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t u) {
   float2 f = make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
   return h2_as_u32(__float22half2_rn(f));
 }
+// A bf16 pair of a BF16 token as an MMA operand: converted to fp16 beside
+// packed tokens (ring steps), as it is in an all-BF16 cache.
+template <int MODE>
+__device__ __forceinline__ uint32_t bf_operand(uint32_t u) {
+  if constexpr (MODE == MLAQ_BF16)
+    return u;
+  else
+    return bf2_to_h2(u);
+}
 
 // Ring slot validity for a sequence of length L. Slot j < 4 holds sink token
 // j. Slot 4 + r holds the newest token t < L with t mod 128 == r, valid iff
@@ -602,7 +611,9 @@ __global__ void __maxnreg__(decode_maxnreg<NH>()) decode_kernel(DecodeParams p) 
   const uint32_t tmem = sm.tmem_base;
   int agg_ctr = 0;    // aggregation steps issued by this CTA
   int page_ctr = -1;  // the last of them that was a page step (reads every A column)
-  constexpr uint32_t kAggIdesc = umma_idesc_f16(128, NH);
+  // aggregation MMA: fp16 V^T and P^T; bf16 for an all-BF16 cache (whose
+  // steps never mix with packed ones)
+  constexpr uint32_t kAggIdesc = MODE == MLAQ_BF16 ? umma_idesc_bf16(128, NH) : umma_idesc_f16(128, NH);
   ProdCursor pc;
   if (tid == 0) {
     producer_init<MODE>(p, pc, first, i0, i1);
@@ -633,7 +644,10 @@ __global__ void __maxnreg__(decode_maxnreg<NH>()) decode_kernel(DecodeParams p) 
     auto ld_q = [&](const uint16_t* src) {
       const uint32_t u = *reinterpret_cast<const uint32_t*>(src);
       qbad |= (u & 0x7fffu) > 0x477fu || ((u >> 16) & 0x7fffu) > 0x477fu;
-      return bf2_to_h2(u);
+      if constexpr (MODE == MLAQ_BF16)
+        return u;  // all-BF16 cache: bf16 score MMAs on the query as given
+      else
+        return bf2_to_h2(u);
     };
 #pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
@@ -646,18 +660,24 @@ __global__ void __maxnreg__(decode_maxnreg<NH>()) decode_kernel(DecodeParams p) 
           const int c = 64 * (2 * w + j) + 16 * kk + 2 * i;
           QF[j][kk][hb][0] = ld_q(ql + (size_t)h * kDL + c);
           QF[j][kk][hb][1] = ld_q(ql + (size_t)h * kDL + c + 8);
-          const float2 a = __half22float2(u32_as_h2(QF[j][kk][hb][0]));
-          const float2 bq = __half22float2(u32_as_h2(QF[j][kk][hb][1]));
-          acc += (a.x + a.y) + (bq.x + bq.y);
+          if constexpr (MODE != MLAQ_BF16) {
+            const float2 a = __half22float2(u32_as_h2(QF[j][kk][hb][0]));
+            const float2 bq = __half22float2(u32_as_h2(QF[j][kk][hb][1]));
+            acc += (a.x + a.y) + (bq.x + bq.y);
+          }
         }
         k2[j][hb] = acc;
       }
       const int c = 16 * w + 2 * i;
       QR[hb][0] = ld_q(qp + (size_t)h * kDR + c);
       QR[hb][1] = ld_q(qp + (size_t)h * kDR + c + 8);
-      const float2 a = __half22float2(u32_as_h2(QR[hb][0]));
-      const float2 bq = __half22float2(u32_as_h2(QR[hb][1]));
-      k2[2][hb] = (a.x + a.y) + (bq.x + bq.y);
+      if constexpr (MODE != MLAQ_BF16) {
+        const float2 a = __half22float2(u32_as_h2(QR[hb][0]));
+        const float2 bq = __half22float2(u32_as_h2(QR[hb][1]));
+        k2[2][hb] = (a.x + a.y) + (bq.x + bq.y);
+      } else {
+        k2[2][hb] = 0.f;
+      }
     }
 #pragma unroll
     for (int j = 0; j < 3; ++j)
@@ -668,14 +688,19 @@ __global__ void __maxnreg__(decode_maxnreg<NH>()) decode_kernel(DecodeParams p) 
         v += __shfl_xor_sync(0xffffffffu, v, 2);
         k2[j][hb] = v;
       }
-    // B fragment of the min-term MMA: rows k = 2j, 2j+1 hold hi/lo of K2_j.
+    // B fragment of the min-term MMA: rows k = 2j, 2j+1 hold hi/lo of K2_j
+    // (an all-BF16 cache has no min term).
 #pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
-      const float v = (i == 0) ? k2[0][hb] : (i == 1) ? k2[1][hb] : k2[2][hb];
-      qbad |= !(fabsf(v) < 65520.f);
-      const __half hi = __float2half_rn(v);
-      const __half lo = __float2half_rn(v - __half2float(hi));
-      KM[hb] = (i < 3) ? h2_as_u32(__halves2half2(hi, lo)) : 0u;
+      if constexpr (MODE != MLAQ_BF16) {
+        const float v = (i == 0) ? k2[0][hb] : (i == 1) ? k2[1][hb] : k2[2][hb];
+        qbad |= !(fabsf(v) < 65520.f);
+        const __half hi = __float2half_rn(v);
+        const __half lo = __float2half_rn(v - __half2float(hi));
+        KM[hb] = (i < 3) ? h2_as_u32(__halves2half2(hi, lo)) : 0u;
+      } else {
+        KM[hb] = 0u;
+      }
     }
     if (__any_sync(0xffffffffu, qbad) && lane == 0) atomicOr(p.status, MLAQ_DEV_RANGE);
   };
@@ -808,6 +833,32 @@ __global__ void __maxnreg__(decode_maxnreg<NH>()) decode_kernel(DecodeParams p) 
     }
   };
 
+  // The score pass of an all-BF16 cache: (s, mn) = (1, 0), so the partial
+  // score is one chain of bf16 MMAs over the warp's 144 channels.
+  auto score_pass_bf16 = [&](const uint32_t (&ch)[2][4][4], const uint32_t (&rf)[4],
+                             const uint32_t (&QF)[2][4][2][2], const uint32_t (&QR)[2][2], int hoff) {
+    float sacc[2][4];
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[hb][e] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        mma16816_bf16(sacc[hb], ch[0][kk], QF[0][kk][hb][0], QF[0][kk][hb][1]);
+        mma16816_bf16(sacc[hb], ch[1][kk], QF[1][kk][hb][0], QF[1][kk][hb][1]);
+      }
+      mma16816_bf16(sacc[hb], rf, QR[hb][0], QR[hb][1]);
+    }
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+      const int h = hoff + 8 * hb + 2 * i;
+      sm.sp[w][h][r] = sacc[hb][0];
+      sm.sp[w][h + 1][r] = sacc[hb][1];
+      sm.sp[w][h][r + 8] = sacc[hb][2];
+      sm.sp[w][h + 1][r + 8] = sacc[hb][3];
+    }
+  };
+
   for (int item_idx = i0; item_idx < i1; ++item_idx) {
     const Item it = p.items[item_idx];
     const int L = it.L;
@@ -928,25 +979,35 @@ __global__ void __maxnreg__(decode_maxnreg<NH>()) decode_kernel(DecodeParams p) 
             for (int kk = 0; kk < 4; ++kk) {
               const int c = 64 * (2 * w + j) + 16 * kk + 2 * i;
               const int e0 = bf16_row_pos(c, r), e1 = bf16_row_pos(c + 8, r);
-              ch[j][kk][0] = v0 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(rx + e0)) : 0u;
-              ch[j][kk][1] = v1 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(ry + e0)) : 0u;
-              ch[j][kk][2] = v0 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(rx + e1)) : 0u;
-              ch[j][kk][3] = v1 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(ry + e1)) : 0u;
+              ch[j][kk][0] = v0 ? bf_operand<MODE>(*reinterpret_cast<const uint32_t*>(rx + e0)) : 0u;
+              ch[j][kk][1] = v1 ? bf_operand<MODE>(*reinterpret_cast<const uint32_t*>(ry + e0)) : 0u;
+              ch[j][kk][2] = v0 ? bf_operand<MODE>(*reinterpret_cast<const uint32_t*>(rx + e1)) : 0u;
+              ch[j][kk][3] = v1 ? bf_operand<MODE>(*reinterpret_cast<const uint32_t*>(ry + e1)) : 0u;
             }
           const int c = kDL + 16 * w + 2 * i;
           const int e0 = bf16_row_pos(c, r), e1 = bf16_row_pos(c + 8, r);
-          rf[0] = v0 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(rx + e0)) : 0u;
-          rf[1] = v1 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(ry + e0)) : 0u;
-          rf[2] = v0 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(rx + e1)) : 0u;
-          rf[3] = v1 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(ry + e1)) : 0u;
+          rf[0] = v0 ? bf_operand<MODE>(*reinterpret_cast<const uint32_t*>(rx + e0)) : 0u;
+          rf[1] = v1 ? bf_operand<MODE>(*reinterpret_cast<const uint32_t*>(ry + e0)) : 0u;
+          rf[2] = v0 ? bf_operand<MODE>(*reinterpret_cast<const uint32_t*>(rx + e1)) : 0u;
+          rf[3] = v1 ? bf_operand<MODE>(*reinterpret_cast<const uint32_t*>(ry + e1)) : 0u;
         }
-        score_pass(mx, my, ch, rf, qf, qr, kmn, 0, 0);
-        if constexpr (NP == 2) {
-          uint32_t q1f[2][4][2][2], q1r[2][2], q1k[2];
-          load_q_frags(q1f, q1r, q1k);
-          score_pass(mx, my, ch, rf, q1f, q1r, q1k, 16, 0);
+        if constexpr (MODE == MLAQ_BF16) {
+          score_pass_bf16(ch, rf, qf, qr, 0);
+          if constexpr (NP == 2) {
+            uint32_t q1f[2][4][2][2], q1r[2][2], q1k[2];
+            load_q_frags(q1f, q1r, q1k);
+            score_pass_bf16(ch, rf, q1f, q1r, 16);
+          }
+        } else {
+          score_pass(mx, my, ch, rf, qf, qr, kmn, 0, 0);
+          if constexpr (NP == 2) {
+            uint32_t q1f[2][4][2][2], q1r[2][2], q1k[2];
+            load_q_frags(q1f, q1r, q1k);
+            score_pass(mx, my, ch, rf, q1f, q1r, q1k, 16, 0);
+          }
         }
-        // dequantize the content tile in place (fp16, one rounding) and
+        // dequantize the content tile in place (fp16, one rounding; bf16
+        // tokens of an all-BF16 cache are the values themselves) and
         // transpose each 8x8 block for the aggregation B operand.
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -954,10 +1015,15 @@ __global__ void __maxnreg__(decode_maxnreg<NH>()) decode_kernel(DecodeParams p) 
           const __half2 s2y = __low2half2(u32_as_h2(my[j])), m2y = __high2half2(u32_as_h2(my[j]));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            ch[j][kk][0] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][0]), s2x, m2x)));
-            ch[j][kk][1] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][1]), s2y, m2y)));
-            ch[j][kk][2] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][2]), s2x, m2x)));
-            ch[j][kk][3] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][3]), s2y, m2y)));
+            if constexpr (MODE == MLAQ_BF16) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) ch[j][kk][e] = movmatrix_t(ch[j][kk][e]);
+            } else {
+              ch[j][kk][0] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][0]), s2x, m2x)));
+              ch[j][kk][1] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][1]), s2y, m2y)));
+              ch[j][kk][2] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][2]), s2x, m2x)));
+              ch[j][kk][3] = movmatrix_t(h2_as_u32(__hfma2(u32_as_h2(ch[j][kk][3]), s2y, m2y)));
+            }
           }
         }
         // content tile -> TMEM A step buffer (lanes = channels, columns = token pairs)
@@ -1028,7 +1094,10 @@ __global__ void __maxnreg__(decode_maxnreg<NH>()) decode_kernel(DecodeParams p) 
             const float p0 = ex2(x0 - mref), p1 = ex2(x1 - mref);
             l_run[hp] = l_run[hp] * alpha + (p0 + p1);
             const int off = (hq >> 3) * 256 + (kp >> 3) * 128 + (hq & 7) * 16 + (kp & 7) * 2;
-            *reinterpret_cast<__half2*>(&sm.pt[ab][off]) = __floats2half2_rn(p0, p1);
+            if constexpr (MODE == MLAQ_BF16)
+              *reinterpret_cast<__nv_bfloat162*>(&sm.pt[ab][off]) = __floats2bfloat162_rn(p0, p1);
+            else
+              *reinterpret_cast<__half2*>(&sm.pt[ab][off]) = __floats2half2_rn(p0, p1);
             if ((lane & 7) == 0) sm.alpha[hq] = alpha;
             rs |= alpha != 1.f;
           }

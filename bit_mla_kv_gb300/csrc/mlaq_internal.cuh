@@ -247,6 +247,13 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// D += A * B, m16n8k16, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma16816_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -341,6 +348,10 @@ __device__ __forceinline__ uint64_t umma_smem_desc(uint32_t saddr, uint32_t k_st
 // Instruction descriptor, kind::f16: fp16 A/B, fp32 D, both K-major.
 __host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// The same with bf16 A and B (both operands always share one type).
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
+  return umma_idesc_f16(M, N) | (1u << 7) | (1u << 10);
 }
 // D (TMEM) (+)= A (TMEM) x B (smem descriptor)^T; issued by one thread.
 __device__ __forceinline__ void umma_f16_ts(uint32_t d_t, uint32_t a_t, uint64_t bdesc, uint32_t idesc, bool acc) {
