@@ -139,7 +139,9 @@ int mlaq_cache_destroy(mlaq_cache* cache);
  * token 128 positions earlier, which from then on is read from its packed
  * copy (no re-quantization). In BF16 mode the BF16 token is stored in the
  * page instead. Invalid page entries set MLAQ_DEV_PAGE_OOB and skip the token.
- * The decode computes on fp16 operands, so the writer checks their range: a
+ * The decode computes on fp16 operands (bf16 for an all-BF16 cache, under the
+ * same bound, which also keeps every score finite in fp32), so the writer
+ * checks their range: a
  * BF16 copy (ring slot or BF16-mode page) holding a value beyond +-65504 or a
  * NaN, or a packed group whose largest reconstructed value mn + (2^b - 1) * s
  * reaches 65520, sets MLAQ_DEV_RANGE (non-finite metadata sets
@@ -162,8 +164,9 @@ int mlaq_append(mlaq_cache* cache, const int32_t* page_table, int32_t* seq_lens,
  * kernel); all tokens share one softmax. L == 0 gives out = 0, lse = -inf.
  * Work is split over the GPU (split-KV) by a device-side planner from
  * seq_lens, and merged by a log-sum-exp combine kernel: three launches, no
- * host sync. The kernel computes on fp16 operands with fp32 accumulation, so
- * inputs must lie in fp16 range; this is checked: a query element beyond
+ * host sync. The kernel computes on fp16 operands (bf16 for an all-BF16
+ * cache) with fp32 accumulation, and inputs must lie in fp16 range in every
+ * mode; this is checked: a query element beyond
  * +-65504 or a NaN, or a per-group (64-channel) sum of one head's query
  * beyond the fp16 range, sets MLAQ_DEV_RANGE (cached tokens are checked by
  * the writer); that sequence's output is then undefined and the other
