@@ -313,6 +313,12 @@ class Workbench:
         torch.cuda.empty_cache()
 
 
+# GB300 datasheet figures (context beside the measured peaks): HBM3e bandwidth
+# and dense bf16 tensor throughput per GPU.
+NOMINAL_HBM_GBS = 7900.0
+NOMINAL_BF16_TFLOPS = 2250.0
+
+
 def roofline_for(wl, mean_lens, kern_ms):
     """Roofline of one mlaq_decode call (plan + decode + combine) for the
     workload at the given (mean) sequence lengths."""
@@ -324,11 +330,13 @@ def roofline_for(wl, mean_lens, kern_ms):
     if t_mem >= t_ten:
         achieved = dec_bytes / (kern_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "peak_source": f"{peak_src} hbm_gbs (copy)"}
+                "peak_source": f"{peak_src} hbm_gbs (copy)",
+                "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS}
     else:
         achieved = flops / (kern_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tf_burst, "unit": "TFLOP/s",
-                "frac": achieved / tf_burst, "peak_source": f"{peak_src} bf16_tflops (burst)"}
+                "frac": achieved / tf_burst, "peak_source": f"{peak_src} bf16_tflops (burst)",
+                "nominal_peak": NOMINAL_BF16_TFLOPS, "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS}
     roof["kernel_ms"] = kern_ms
     roof["roofline_us"] = max(t_mem, t_ten) * 1e6
     roof["algorithmic_bytes"] = dec_bytes
@@ -405,7 +413,7 @@ def run_per_config(names, K, Wm, l2_flush, ws, rank, device, local, variant=0):
         res[name] = {"workload": wl.description, "steps": K, "warmup": Wm,
                      "step_us": m["ms_max"] * 1e3, "GB/s": m["value"],
                      "decode_call_us": m["kern_avg"] * 1e3, "append_us": m["append_ms"] * 1e3,
-                     "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac", "roofline_us")},
+                     "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac", "roofline_us", "frac_of_nominal")},
                      "writer_prefill_GB/s": pre["GB/s"], "clocks": clocks}
         wb.release()
     return res
