@@ -969,27 +969,26 @@ __global__ void __maxnreg__(decode_maxnreg<NH>()) decode_kernel(DecodeParams p) 
             mx[j] = v0 ? one : 0u;
             my[j] = v1 ? one : 0u;
           }
-          // rows lr and lr + 8 share lr mod 8 = r, so both use the chunk
-          // permutation of r; channels c and c + 8 are adjacent chunks
-          const uint16_t* rx = reinterpret_cast<const uint16_t*>(st + lr * (kD * 2));
-          const uint16_t* ry = reinterpret_cast<const uint16_t*>(st + (lr + 8) * (kD * 2));
+          // One ldmatrix.x4 per 16 x 16 fragment: lane L gives the address of
+          // row 8 (L / 8 % 2) + L % 8 of the step at the 16-byte chunk q + L / 16
+          // (channels 8q .. 8q + 7, q = (16-channel block) / 8); rows keep their
+          // chunks XOR-permuted by the row index mod 8, so each 8 x 8 matrix
+          // reads eight distinct bank groups. The registers come back in the
+          // A-fragment order: rows r / r + 8, channels 2i, 2i + 1 (+ 8).
+          const int mrow = s * kT + 8 * ((lane >> 3) & 1) + (lane & 7);
+          const uint32_t rowa = smem_u32(st + mrow * (kD * 2));
+          auto frag = [&](int q, uint32_t (&f)[4]) {
+            ldmatrix_x4(rowa + ((uint32_t)((q + (lane >> 4)) ^ (lane & 7)) << 4), f);
+            f[0] = v0 ? bf_operand<MODE>(f[0]) : 0u;
+            f[1] = v1 ? bf_operand<MODE>(f[1]) : 0u;
+            f[2] = v0 ? bf_operand<MODE>(f[2]) : 0u;
+            f[3] = v1 ? bf_operand<MODE>(f[3]) : 0u;
+          };
 #pragma unroll
           for (int j = 0; j < 2; ++j)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const int c = 64 * (2 * w + j) + 16 * kk + 2 * i;
-              const int e0 = bf16_row_pos(c, r), e1 = bf16_row_pos(c + 8, r);
-              ch[j][kk][0] = v0 ? bf_operand<MODE>(*reinterpret_cast<const uint32_t*>(rx + e0)) : 0u;
-              ch[j][kk][1] = v1 ? bf_operand<MODE>(*reinterpret_cast<const uint32_t*>(ry + e0)) : 0u;
-              ch[j][kk][2] = v0 ? bf_operand<MODE>(*reinterpret_cast<const uint32_t*>(rx + e1)) : 0u;
-              ch[j][kk][3] = v1 ? bf_operand<MODE>(*reinterpret_cast<const uint32_t*>(ry + e1)) : 0u;
-            }
-          const int c = kDL + 16 * w + 2 * i;
-          const int e0 = bf16_row_pos(c, r), e1 = bf16_row_pos(c + 8, r);
-          rf[0] = v0 ? bf_operand<MODE>(*reinterpret_cast<const uint32_t*>(rx + e0)) : 0u;
-          rf[1] = v1 ? bf_operand<MODE>(*reinterpret_cast<const uint32_t*>(ry + e0)) : 0u;
-          rf[2] = v0 ? bf_operand<MODE>(*reinterpret_cast<const uint32_t*>(rx + e1)) : 0u;
-          rf[3] = v1 ? bf_operand<MODE>(*reinterpret_cast<const uint32_t*>(ry + e1)) : 0u;
+            for (int kk = 0; kk < 4; ++kk) frag(8 * (2 * w + j) + 2 * kk, ch[j][kk]);
+          frag(kDL / 8 + 2 * w, rf);
         }
         if constexpr (MODE == MLAQ_BF16) {
           score_pass_bf16(ch, rf, qf, qr, 0);

@@ -235,6 +235,14 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t
 
 // Pure register operations: not volatile, so independent ones can be
 // interleaved by the compiler.
+// Four 8x8 b16 matrices from shared memory in the mma fragment layout; lane
+// L gives the 16-byte row address of row L % 8 of matrix L / 8.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t saddr, uint32_t (&f)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(f[0]), "=r"(f[1]), "=r"(f[2]), "=r"(f[3])
+               : "r"(saddr)
+               : "memory");
+}
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
   uint32_t d;
   asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
