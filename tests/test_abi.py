@@ -40,6 +40,16 @@ def test_binding_covers_the_exports():
     assert sorted(m.EXPORTED) == declared_functions()
 
 
+def test_binding_status_bits_match_the_header():
+    import bit_mla_kv_gb300.mlaq as m
+    text = open(HEADER).read()
+    bits = dict(re.findall(r"#define MLAQ_DEV_([A-Z_]+) (0x[0-9a-fA-F]+)", text))
+    assert len(bits) >= 6
+    for name, val in bits.items():
+        assert getattr(m, "DEV_" + name) == int(val, 16), name
+    assert len(set(bits.values())) == len(bits)   # distinct bits
+
+
 def test_buffer_sizes_host_logic(lib):
     import bit_mla_kv_gb300.mlaq as m
     cb, mb, rb, wb = m.buffer_sizes("C4R4", 10, 3, 16)
