@@ -15,12 +15,14 @@
 // a sequence with one item is finalized by the attention kernel, otherwise
 // the combine kernel merges its items' normalized partials.
 //
-// Attention (one CTA = NH = 16 or 32 heads, 4 warps, 2 CTAs per SM):
+// Attention (one CTA = NH = 16 or 32 heads, 4 warps; three 16-head or two
+// 32-head CTAs per SM):
 //  * Pages (codes + fp16 meta) or ring chunks are staged by bulk copies
-//    (TMA) into a shared-memory ring (4 stages, 2 for 32-head CTAs) that runs
-//    ahead across items; every wait is bounded in wall time.
-//  * A packed page is one step of four 16-token sub-steps under one pair of
-//    barriers; ring chunks and BF16 page quarters are 16-token steps.
+//    (TMA) into a 2-stage shared-memory ring per CTA that runs ahead across
+//    items; every wait is bounded in wall time.
+//  * A packed page is one body of four 16-token sub-steps (32-head CTAs) or
+//    two bodies of two (16-head CTAs), each under one pair of barriers; ring
+//    chunks and BF16 page quarters are 16-token steps.
 //  * Warp w owns content groups 2w, 2w+1 (channels 128w..128w+127) and RoPE
 //    channels 16w..16w+15.
 //  * Scores use exact integer codes as fp16 MMA operands: per group g,
@@ -36,8 +38,10 @@
 //    mn, one rounding), transposed in registers with movmatrix and stored to
 //    TMEM (lanes = channels); one tcgen05.mma per sub-step and channel block
 //    accumulates O^T += V^T P^T in TMEM while the warps unpack the next page.
-//  * BF16 tokens (ring and the all-BF16 cache) take the same path with
-//    (s, mn) = (1, 0).
+//  * BF16 ring tokens of a packed cache take the same path with
+//    (s, mn) = (1, 0); an all-BF16 cache runs both contractions on its bf16
+//    values as given (bf16 register MMAs for the scores, bf16 tcgen05
+//    operands for the aggregation).
 #include <math.h>
 
 #include <atomic>
