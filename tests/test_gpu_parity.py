@@ -363,6 +363,31 @@ def test_decode_more_heads(mode, H):
             assert_close_out(out[b], lse[b], ro, rl, f"{mode} H={H} ctas={ctas} seq {b}")
 
 
+@pytest.mark.parametrize("seed", range(24))
+def test_random_batches_against_oracle(seed):
+    # Seeded random batches: mode, head count (every blocking: 16-head and
+    # 32-head CTAs), kernel variant, CTA count and a mix of empty, short,
+    # ring-only, page-edge and longer sequences; every sequence is checked.
+    rng = np.random.default_rng(1000 + seed)
+    mode = ["C4R4", "C2R4", "BF16"][seed % 3]
+    H = int(rng.choice([16, 32, 48, 64, 128]))
+    B = int(rng.integers(1, 24))
+    pool = [0, 1, 3, 4, 5, 63, 64, 65, 127, 131, 132, 133, 200, 256, 257, 700, 1000, 2049, 4097]
+    lens = [int(rng.choice(pool)) if rng.random() < 0.7 else int(rng.integers(1, 6000)) for _ in range(B)]
+    case = Case(mode, lens, H, seed=2000 + seed)
+    case.build()
+    ctas = [None, 1, int(rng.integers(2, 1025))][int(rng.integers(0, 3))]
+    if ctas is not None:
+        case.cache.set_decode_ctas(ctas)
+    variant = int(rng.choice([0, 0, 2]))
+    case.cache.set_decode_variant(variant)
+    out, lse = case.decode()
+    assert case.cache.device_status() == 0
+    for b in range(case.B):
+        ro, rl = case.oracle_seq(b)
+        assert_close_out(out[b], lse[b], ro, rl, f"seed {seed} {mode} H={H} ctas={ctas} v={variant} seq {b} L={lens[b]}")
+
+
 @pytest.mark.parametrize("mode,where", [("C4R4", "ring"), ("C4R4", "packed"), ("C2R4", "ring_small_append"),
                                         ("BF16", "page")])
 def test_fp16_range_is_checked_for_tokens(mode, where):
