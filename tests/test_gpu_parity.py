@@ -363,6 +363,54 @@ def test_decode_more_heads(mode, H):
             assert_close_out(out[b], lse[b], ro, rl, f"{mode} H={H} ctas={ctas} seq {b}")
 
 
+@pytest.mark.parametrize("seed", range(8))
+def test_random_append_schedules_bit_exact(seed):
+    # Each sequence's tokens arrive in a random schedule of varlen appends
+    # (zero, one or many rows per sequence per call: both the one-CTA-per-row
+    # and the bulk writer, ring retirement, page edges); afterwards every
+    # code, meta word and ring slot equals the oracle's for the whole
+    # sequence, as if it had been appended at once.
+    from bit_mla_kv_gb300.mlaq import Cache
+    rng = np.random.default_rng(3000 + seed)
+    mode = ["C4R4", "C2R4"][seed % 2]
+    B = int(rng.integers(1, 16))
+    ncalls = int(rng.integers(2, 6))
+    counts = rng.integers(0, 400, size=(ncalls, B)) * (rng.random((ncalls, B)) < 0.8)
+    counts[rng.random((ncalls, B)) < 0.2] = 1
+    lens = [int(x) for x in counts.sum(0)]
+    case = Case(mode, lens, 16, seed=4000 + seed)
+    case.cache = Cache(mode, case.num_pages, case.B, case.page_table.shape[1], max_heads=16)
+    case.pt_d = case.page_table.cuda()
+    case.seq_d = torch.zeros(case.B, dtype=torch.int32, device="cuda")
+    done = [0] * B
+    for call in range(ncalls):
+        cnt = [int(x) for x in counts[call]]
+        if sum(cnt) == 0:
+            continue
+        rows = torch.cat([torch.arange(int(case.cu[b]) + done[b], int(case.cu[b]) + done[b] + cnt[b])
+                          for b in range(B)])
+        cu = torch.zeros(B + 1, dtype=torch.int32)
+        cu[1:] = torch.cumsum(torch.tensor(cnt), 0)
+        case.cache.append(case.pt_d, case.seq_d, case.c[rows].cuda().contiguous(), case.k[rows].cuda().contiguous(),
+                          cu_new=cu.cuda())
+        done = [d + c for d, c in zip(done, cnt)]
+    assert case.cache.device_status() == 0
+    assert case.seq_d.cpu().tolist() == lens
+    codes, meta = _export_all(case)
+    ring = case.cache.ring_view().float().cpu().numpy()
+    off = 0
+    for b, L in enumerate(lens):
+        if L == 0:
+            continue
+        ec, em = expected_codes(case, b)
+        np.testing.assert_array_equal(codes[off:off + L], ec, err_msg=f"seed {seed} codes seq {b}")
+        np.testing.assert_array_equal(meta[off:off + L].view(np.uint16), em.view(np.uint16),
+                                      err_msg=f"seed {seed} meta seq {b}")
+        off += L
+        er, valid = O.expected_ring(case.tokens(b), L)
+        np.testing.assert_array_equal(ring[b][valid], er[valid], err_msg=f"seed {seed} ring seq {b}")
+
+
 @pytest.mark.parametrize("seed", range(24))
 def test_random_batches_against_oracle(seed):
     # Seeded random batches: mode, head count (every blocking: 16-head and
