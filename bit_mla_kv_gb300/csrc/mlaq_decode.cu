@@ -802,6 +802,10 @@ __global__ void __maxnreg__(decode_maxnreg<NH>()) decode_kernel(DecodeParams p) 
       for (int hb = 0; hb < 2; ++hb)
 #pragma unroll
         for (int e = 0; e < 4; ++e) d0[hb][e] = d1[hb][e] = d2[hb][e] = 0.f;
+      // the RoPE term first: its segment is unpacked before the content
+      // (onedev.kr "어떻게 쓰나": RoPE QK scheduled early)
+      mma16816(d2[0], rf, QR[0][0], QR[0][1]);
+      mma16816(d2[1], rf, QR[1][0], QR[1][1]);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         mma16816(d0[0], ch[0][kk], QF[0][kk][0][0], QF[0][kk][0][1]);
@@ -809,8 +813,6 @@ __global__ void __maxnreg__(decode_maxnreg<NH>()) decode_kernel(DecodeParams p) 
         mma16816(d0[1], ch[0][kk], QF[0][kk][1][0], QF[0][kk][1][1]);
         mma16816(d1[1], ch[1][kk], QF[1][kk][1][0], QF[1][kk][1][1]);
       }
-      mma16816(d2[0], rf, QR[0][0], QR[0][1]);
-      mma16816(d2[1], rf, QR[1][0], QR[1][1]);
       float sxv[3], syv[3];
 #pragma unroll
       for (int j = 0; j < 3; ++j) {
@@ -1173,6 +1175,19 @@ __global__ void __maxnreg__(decode_maxnreg<NH>()) decode_kernel(DecodeParams p) 
             mx[j] = v0 ? mxr : 0u;
             my[j] = v1 ? myr : 0u;
           }
+          uint32_t rf[4];  // the RoPE slice first (its MMAs lead the score pass)
+          {
+            uint32_t ax = *reinterpret_cast<const uint32_t*>(st + lr * CB + ROPE_OFF + 4 * (2 * w + (i >> 1)));
+            uint32_t ay = *reinterpret_cast<const uint32_t*>(st + (lr + 8) * CB + ROPE_OFF + 4 * (2 * w + (i >> 1)));
+            if (i & 1) {
+              ax >>= 8;
+              ay >>= 8;
+            }
+            rf[0] = int4_pos(ax, 0u, 0);
+            rf[1] = int4_pos(ay, 0u, 0);
+            rf[2] = int4_pos(ax, 0u, 1);
+            rf[3] = int4_pos(ay, 0u, 1);
+          }
           uint32_t ch[2][4][4];
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
@@ -1202,19 +1217,6 @@ __global__ void __maxnreg__(decode_maxnreg<NH>()) decode_kernel(DecodeParams p) 
                 ch[j][kk][3] = int2_pos(ay, ay8, 2 * kk + 1);
               }
             }
-          }
-          uint32_t rf[4];
-          {
-            uint32_t ax = *reinterpret_cast<const uint32_t*>(st + lr * CB + ROPE_OFF + 4 * (2 * w + (i >> 1)));
-            uint32_t ay = *reinterpret_cast<const uint32_t*>(st + (lr + 8) * CB + ROPE_OFF + 4 * (2 * w + (i >> 1)));
-            if (i & 1) {
-              ax >>= 8;
-              ay >>= 8;
-            }
-            rf[0] = int4_pos(ax, 0u, 0);
-            rf[1] = int4_pos(ay, 0u, 0);
-            rf[2] = int4_pos(ax, 0u, 1);
-            rf[3] = int4_pos(ay, 0u, 1);
           }
           score_pass(mx, my, ch, rf, qf, qr, kmn, 0, 16 * sub);
           if constexpr (NP == 2) {
